@@ -15,9 +15,9 @@
  * Sources (cited by page title and section):
  *  [BW]  "8-bit Optimizers via Block-wise Quantization" -- innovations list
  *        (dynamic tree quantization extended to unipolar data) and method
- *        bullets (2048-element blocks, absmax normaliser, divide then binary
- *        search to an 8-bit index, lookup-table dequantization, update done
- *        in 32 bit in registers).
+ *        bullets (2048-element blocks, absmax normaliser, normalise then
+ *        binary search to an 8-bit index, lookup-table dequantization, update
+ *        done in 32 bit in registers).
  *  [SR]  "Stochastic rounding support for 8-bit optimizers" -- feature
  *        request (round the BF16 parameter update up or down with a chance
  *        set by the rounding error; no FP32 master weights) and the scoping
@@ -128,9 +128,11 @@ int q8o_zero_code(int kind) { return kind == Q8O_UNSIGNED ? 0 : 127; }
 
 /* ------------------------------------------------------------------------ */
 /* Quantization.  [BW] method bullets: divide by the block maximum, then map */
-/* to an 8-bit index by binary search.  Reading: the index is the number of  */
-/* decision thresholds strictly below the normalised value, so a value that  */
-/* sits exactly on a threshold takes the lower code.                         */
+/* to an 8-bit index by binary search.  Readings: the division by the block  */
+/* constant M is a multiplication by the correctly rounded reciprocal 1/M,   */
+/* clamped to [-1, 1] (the product can pass 1 by an ulp); the index is the   */
+/* number of decision thresholds strictly below the normalised value, so a   */
+/* value that sits exactly on a threshold takes the lower code.              */
 /* ------------------------------------------------------------------------ */
 
 static int bisect_thresholds(const float mid[255], float x)
@@ -174,9 +176,12 @@ static void quantize_block(const float mid[255], int zero_code,
 {
     float M = block_absmax(x, n);
     *absmax = M;
+    float inv = M > 0.0f ? 1.0f / M : 0.0f;
     for (int64_t i = 0; i < n; ++i) {
         if (M == 0.0f) { codes[i] = (uint8_t)zero_code; continue; }
-        float y = x[i] / M;                      /* |y| <= 1 since |x| <= M */
+        float y = x[i] * inv;
+        if (y > 1.0f) y = 1.0f;
+        if (y < -1.0f) y = -1.0f;
         codes[i] = (uint8_t)bisect_thresholds(mid, y);
     }
 }
