@@ -1,0 +1,412 @@
+#!/usr/bin/env python
+"""Benchmark of the fused 8-bit blockwise AdamW + stochastic-rounding step.
+
+One "step" is one adamw8bit_sr_step call over the whole tensor list of the
+workload (default: the GPT-Neo 6.7B-shaped list, 6,658,011,136 bf16 params,
+8-bit m/v with per-2048 absmax), with every input resident in HBM.  Inputs
+(66.6 GB of traffic per step) are far larger than the 129 MB L2, so no flush
+is needed between steps.  Prints one JSON line.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+--impl reference times the CPU oracle (the plain C restatement of the method,
+single-threaded) on a bounded sample of the same workload.
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "fused AdamW8bit+SR step: Gparams/s and HBM GB/s (% of peak), 1 GB300"
+UNIT = "Gparams/s"
+BLOCK = 2048
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="gptneo-6.7b")
+    ap.add_argument("--flat", type=int, default=0,
+                    help="replace the workload by one flat tensor of this many params (profiling)")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--cpu-blocks", type=int, default=24000,
+                    help="2048-blocks in the oracle's timed sample (about 10-20 s on one core)")
+    return ap.parse_args()
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def workload(args):
+    from bit_blockwise_adamw_gb300 import workloads as W
+    if args.flat:
+        return W.custom("flat-%d" % args.flat, [args.flat], steps=args.steps, grad_std=1e-4,
+                        outlier_rate=1e-4, outlier_factor=1000.0,
+                        hp=dict(lr=6e-4, weight_decay=0.1), data_seed=1003)
+    return W.WORKLOADS[args.workload]
+
+
+def algorithmic_bytes(wl):
+    """Bytes the step must move: 8-bit path 10 B/param (grad 2, param 2+2,
+    codes 1+1 each way) + 16 B per block (two absmax read and written);
+    fp32-state path 22 B/param; BF16-state path 14 B/param."""
+    total = 0
+    for t in wl.tensors:
+        if wl.state == "bf16":
+            total += 14 * t.numel
+        elif t.numel >= 4096:
+            total += 10 * t.numel + 16 * ((t.numel + BLOCK - 1) // BLOCK)
+        else:
+            total += 22 * t.numel
+    return total
+
+
+def launches_per_step(wl):
+    n_big = sum(1 for t in wl.tensors if t.numel >= 4096 or wl.state == "bf16")
+    n_small = sum(1 for t in wl.tensors if t.numel < 4096 and wl.state != "bf16")
+    per = 448
+    return (n_big + per - 1) // per + (n_small + per - 1) // per
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled while the timed region runs."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.out = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.QUERY,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.out, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.flush()
+        rows = []
+        with open(self.out.name) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.out.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({n for r in rows for n, v in zip(names, r[5:9]) if v.lower() == "active"})
+        busy = [s for s in sm if s > 0.5 * max(sm)] if sm else []
+        return {"sm_mhz": statistics.median(busy or sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+def traffic_per_launch(kernel, units):
+    """DRAM bytes per launch from the committed ncu summary of this kernel,
+    scaled to `units` params, or None if the kernel source changed since."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "dram_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)[kernel]
+    except (OSError, KeyError, ValueError):
+        return None
+    h = hashlib.sha256()
+    for rel in d["sources"]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    if h.hexdigest() != d["sources_sha256"]:
+        return None
+    return d["dram_bytes_per_param"] * units
+
+
+# ---------------------------------------------------------------- CPU oracle
+
+def oracle_sample_time(wl, nblocks, seed=0):
+    """Time the oracle (single-threaded C) on a seeded sample of the
+    workload's 2048-blocks for one step; returns (params, seconds)."""
+    import oracle as o
+    from bit_blockwise_adamw_gb300 import workloads as W
+    rng = np.random.default_rng(seed)
+    bigs = [i for i, t in enumerate(wl.tensors) if t.numel >= 4096 or wl.state == "bf16"]
+    sizes = np.array([wl.tensors[i].numel for i in bigs], np.float64)
+    pick = rng.choice(len(bigs), size=nblocks, p=sizes / sizes.sum())
+    # inputs of the sample: N(0, 0.02) params and the workload's grad law
+    gen = torch.Generator().manual_seed(seed)
+    p = (torch.randn(nblocks * BLOCK, generator=gen) * 0.02).to(torch.bfloat16)
+    g = (torch.randn(nblocks * BLOCK, generator=gen) * wl.grad_std).to(torch.bfloat16)
+    p = p.view(torch.int16).numpy().view(np.uint16).reshape(nblocks, BLOCK)
+    g = g.view(torch.int16).numpy().view(np.uint16).reshape(nblocks, BLOCK)
+    offs = W.philox_offsets(wl)
+    h = dict(wl.hp)
+    hp = o.hparams(lr=h["lr"], beta1=h["beta1"], beta2=h["beta2"], eps=h["eps"],
+                   weight_decay=h["weight_decay"], step=1, seed=wl.philox_seed)
+    if wl.state == "bf16":
+        states = [o.State16(p[k].copy(), g[k].copy(), np.zeros(BLOCK, np.uint16), np.zeros(BLOCK, np.uint16))
+                  for k in range(nblocks)]
+    else:
+        states = [o.State8.zeros(p[k].copy(), g[k].copy()) for k in range(nblocks)]
+    e0 = [offs[bigs[pick[k]]] for k in range(nblocks)]
+    t0 = time.perf_counter()
+    for k, s in enumerate(states):
+        if wl.state == "bf16":
+            o.adamw_bf16_tensor(s, e0[k], hp)
+        else:
+            o.adamw8bit_tensor(s, e0[k], hp)
+    dt = time.perf_counter() - t0
+    return nblocks * BLOCK, dt
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return 0
+    wl = workload(args)
+    # each step: a bounded sample of the workload (bounded so K+W steps stay within minutes)
+    nblocks = max(64, min(args.cpu_blocks, 2000))
+    times = []
+    units = 0
+    for i in range(args.warmup + args.steps):
+        n, dt = oracle_sample_time(wl, nblocks, seed=i)
+        if i >= args.warmup:
+            times.append(dt)
+            units += n
+    total = sum(times)
+    value = units / total / 1e9
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / max(1, args.steps),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": {"workload": wl.name, "sample_blocks_per_step": nblocks},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "%d seeded 2048-blocks of %s per step, one step each" % (nblocks, wl.name)},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------- GPU arm
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+
+    from bit_blockwise_adamw_gb300 import build as B
+    B.build()
+    import bit_blockwise_adamw_gb300 as q8
+    from bit_blockwise_adamw_gb300 import workloads as W
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    wl = workload(args)
+    q8.q8_prepare_device()
+    params = W.init_params(wl, device)
+    grads = W.make_grads(wl, 1, device)
+    if wl.state == "bf16":
+        states = [q8.Tensor16(p, g, torch.zeros_like(p), torch.zeros_like(p)) for p, g in zip(params, grads)]
+        packed = q8.pack_tensor16(states)
+        step_fn = q8.adamw_bf16_sr_step
+    else:
+        states = [q8.Tensor8.zeros_like(p, g) for p, g in zip(params, grads)]
+        packed = q8.pack_tensor8(states)
+        step_fn = q8.adamw8bit_sr_step
+    numel = wl.numel
+    h = dict(wl.hp)
+
+    def hp(t):
+        return q8.hparams(lr=h["lr"], beta1=h["beta1"], beta2=h["beta2"], eps=h["eps"],
+                          weight_decay=h["weight_decay"], step=t, seed=wl.philox_seed)
+
+    stream = torch.cuda.current_stream(device)
+    t = 0
+    for _ in range(args.warmup):
+        t += 1
+        step_fn(packed, hp(t), stream)
+    torch.cuda.synchronize(device)
+
+    # timed region: K steps, one event pair per step on the launching stream
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    clocks = ClockSampler(local)
+    clocks.start()
+    barrier()
+    torch.cuda.synchronize(device)
+    start.record(stream)
+    for k in range(args.steps):
+        t += 1
+        ev[k][0].record(stream)
+        step_fn(packed, hp(t), stream)
+        ev[k][1].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize(device)
+    barrier()
+    clock_info = clocks.stop()
+    total_ms = start.elapsed_time(stop)
+    per = [a.elapsed_time(b) for a, b in ev]
+    if world > 1:
+        tt = torch.tensor([total_ms], device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms_per_step = total_ms / args.steps
+    value = world * numel * args.steps / (total_ms / 1e3) / 1e9
+
+    # roofline of the dominant kernel (the fused step kernel: one launch per step here)
+    peak, peak_kind = load_peaks()
+    abytes = algorithmic_bytes(wl)
+    nl = launches_per_step(wl)
+    mean_ms = statistics.mean(per)
+    achieved = abytes / (mean_ms / 1e3) / 1e9
+    kernel = "step16_kernel" if wl.state == "bf16" else "step8_kernel"
+    traffic = traffic_per_launch(kernel, numel / nl) if nl == 1 else None
+    roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                "frac": achieved / peak, "traffic": traffic, "kernel": kernel,
+                "algorithmic_bytes_per_launch": abytes / nl, "peak_source": peak_kind,
+                "median_ms_per_step": statistics.median(per), "min_ms_per_step": min(per)}
+
+    # end to end through the public API: grads in from pinned host memory,
+    # step, updated params back to pinned host memory, every step
+    e2e = None
+    if not args.no_e2e:
+        e2e = run_e2e(args, wl, states, step_fn, hp, t, device, world, barrier)
+        t += args.e2e_steps + 1
+
+    cpu = None
+    if not args.no_cpu_baseline and rank == 0:
+        n, dt = oracle_sample_time(wl, args.cpu_blocks)
+        cpu = {"value": n / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": "%d seeded 2048-blocks (%d params) of %s, one step, single-threaded C oracle"
+                         % (args.cpu_blocks, n, wl.name)}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": wl.name, "params": numel, "tensors": len(wl.tensors),
+                       "blocks": wl.blocks(), "state": wl.state,
+                       "bytes_per_step": abytes, "gbs": abytes / (ms_per_step / 1e3) / 1e9,
+                       "l2": "inputs larger than L2 (%.1f GB moved per step, no flush)" % (abytes / 1e9),
+                       "parallelism": "replicas x%d (each GPU steps its own full list)" % world},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "gpu_launches": nl * args.steps, "clocks": clock_info,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def run_e2e(args, wl, states, step_fn, hp, t, device, world, barrier):
+    """Per step: H2D copy of this step's grads from pinned host memory, the
+    step through the C ABI, D2H copy of the updated params into pinned host
+    memory.  The list is cut into chunks (explicit Philox offsets keep the
+    bits identical to one call) so the copies of one chunk overlap the step of
+    another on three streams."""
+    import bit_blockwise_adamw_gb300 as q8
+    from bit_blockwise_adamw_gb300 import workloads as W
+    offs = W.philox_offsets(wl)
+    for s, off in zip(states, offs):
+        s.philox_offset = off
+    nchunks = min(8, len(states))
+    bounds = np.linspace(0, len(states), nchunks + 1).astype(int)
+    chunks = [list(range(bounds[c], bounds[c + 1])) for c in range(nchunks) if bounds[c + 1] > bounds[c]]
+    host_g = [torch.empty(s.param.numel(), dtype=torch.bfloat16, pin_memory=True) for s in states]
+    host_p = [torch.empty(s.param.numel(), dtype=torch.bfloat16, pin_memory=True) for s in states]
+    for hg, s in zip(host_g, states):
+        hg.copy_(s.grad)
+    packs = [(q8.pack_tensor16 if wl.state == "bf16" else q8.pack_tensor8)([states[i] for i in c]) for c in chunks]
+    s_in, s_cmp, s_out = (torch.cuda.Stream(device) for _ in range(3))
+
+    def one_step(tt):
+        for c, pk in zip(chunks, packs):
+            e_in = torch.cuda.Event()
+            with torch.cuda.stream(s_in):
+                for i in c:
+                    states[i].grad.copy_(host_g[i], non_blocking=True)
+                e_in.record(s_in)
+            s_cmp.wait_event(e_in)
+            step_fn(pk, hp(tt), s_cmp)
+            e_c = torch.cuda.Event()
+            e_c.record(s_cmp)
+            s_out.wait_event(e_c)
+            with torch.cuda.stream(s_out):
+                for i in c:
+                    host_p[i].copy_(states[i].param, non_blocking=True)
+
+    one_step(t + 1)                      # warm-up
+    torch.cuda.synchronize(device)
+    barrier()
+    t0 = time.perf_counter()
+    for k in range(args.e2e_steps):
+        one_step(t + 2 + k)
+    torch.cuda.synchronize(device)
+    barrier()
+    dt = time.perf_counter() - t0
+    if world > 1:
+        tt = torch.tensor([dt], device=device)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        dt = float(tt.item())
+    nb = 2 * wl.numel
+    for s in states:
+        s.philox_offset = -1
+    return {"value": world * wl.numel * args.e2e_steps / dt / 1e9, "unit": UNIT,
+            "h2d_bytes_per_step": nb, "d2h_bytes_per_step": nb, "steps": args.e2e_steps,
+            "ms_per_step": 1e3 * dt / args.e2e_steps,
+            "note": "pinned host grads in, params out, %d chunks on 3 streams" % len(chunks)}
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,128 @@
+// q8_internal.h -- declarations shared by the library's translation units:
+// table layout, kernel argument blocks and host-side launchers.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "q8adamw.h"
+
+namespace q8 {
+
+// Blocking ("8-bit Optimizers via Block-wise Quantization", method bullets:
+// 2048-element blocks).  A CTA of 256 threads owns one block per iteration,
+// eight contiguous elements per thread, so each thread makes one 16-byte load
+// of bf16 data, one 8-byte load of codes and one Philox call.
+constexpr int kBlock = 2048;
+constexpr int kThreads = 256;
+constexpr int kVec = 8;
+static_assert(kThreads * kVec == kBlock, "one block per CTA iteration");
+constexpr int kWarps = kThreads / 32;
+constexpr int kSmall = 4096;
+
+// Search cells.  |x| <= 1 is split into cells by its binade and the top seven
+// mantissa bits (every 2^16 consecutive bit patterns share a cell); magnitudes
+// below 2^-L form cell 0.  L is chosen so that no midpoint lies in cell 0 and
+// the seven mantissa bits keep at most one midpoint in any cell, so the code
+// is   base(cell) + (x beyond the cell's midpoint).
+// Entry layout (uint32): bits 0..7 = base code, bits 16..31 = the low 16 bits
+// of the in-cell midpoint's magnitude (complemented for the negative half),
+// 0xFFFF when the cell holds no midpoint.
+constexpr int kCellShift = 16;
+constexpr int kSignedL = 21;      // smallest signed midpoint is 5e-7 > 2^-21
+constexpr int kUnsignedL = 25;    // smallest unsigned midpoint is 5e-8 > 2^-25
+constexpr int kCellsSigned = 2 + kSignedL * 128;     // per sign
+constexpr int kCellsUnsigned = 2 + kUnsignedL * 128; // non-negative half only
+
+struct DevTables {
+    float cs[256];                         // signed codebook (dequantize m)
+    float cu[256];                         // unsigned codebook (dequantize v)
+    uint32_t cell_s[2 * kCellsSigned];     // [sign][cell]
+    uint32_t cell_u[kCellsUnsigned];       // non-negative x only
+};
+
+// Step scalars formed on the host in double and rounded once to float.
+struct Scalars {
+    float b1, omb1, b2, omb2, eps_t, step_size, decay;
+    uint32_t k0, k1, step;
+    int32_t sr;
+};
+
+// Tensor lists travel as kernel parameters (no device allocation, no copy):
+// at most kMaxList tensors per launch; longer lists take several launches.
+constexpr int kMaxList = 448;
+
+struct Desc8 {                 // one 8-bit-state tensor, 64 bytes
+    uint16_t* p;
+    const uint16_t* g;
+    uint8_t* mq;
+    uint8_t* vq;
+    float* ma;
+    float* va;
+    int64_t n;
+    uint64_t e0;               // Philox index of element 0
+};
+
+struct Step8Args {
+    Scalars s;
+    const DevTables* tab;
+    int32_t nt;
+    int32_t nblocks;                      // total 2048-blocks in this launch
+    int32_t blk_start[kMaxList + 1];      // first global block of each tensor
+    Desc8 d[kMaxList];
+};
+
+struct Desc32 {                // one fp32-state tensor (numel < 4096)
+    uint16_t* p;
+    const uint16_t* g;
+    float* m;
+    float* v;
+    int64_t n;
+    uint64_t e0;
+};
+
+struct Step32Args {
+    Scalars s;
+    int32_t nt;
+    Desc32 d[kMaxList];
+};
+
+struct Desc16 {                // one bf16-state tensor
+    uint16_t* p;
+    const uint16_t* g;
+    uint16_t* m;
+    uint16_t* v;
+    int64_t n;
+    uint64_t e0;
+};
+
+struct Step16Args {
+    Scalars s;
+    int32_t nt;
+    int32_t nblocks;
+    int32_t blk_start[kMaxList + 1];
+    Desc16 d[kMaxList];
+};
+
+static_assert(sizeof(Step8Args) <= 32764, "kernel parameter space");
+static_assert(sizeof(Step16Args) <= 32764, "kernel parameter space");
+static_assert(sizeof(Step32Args) <= 32764, "kernel parameter space");
+
+// Host-side table construction (q8_tables.cu).
+void build_codebook(int kind, float out[256]);
+// Device copy of the tables for the current device, set up on first use.
+cudaError_t device_tables(const DevTables** out);
+
+// Launchers (one per kernel; each returns cudaGetLastError()).
+int resident_ctas(const void* kernel, int threads, size_t smem);
+cudaError_t launch_step8(const Step8Args& a, cudaStream_t st);
+cudaError_t launch_step32(const Step32Args& a, cudaStream_t st);
+cudaError_t launch_step16(const Step16Args& a, cudaStream_t st);
+cudaError_t launch_quantize(const float* x, uint8_t* codes, float* absmax, int64_t n, int kind,
+                            const DevTables* tab, cudaStream_t st);
+cudaError_t launch_dequantize(const uint8_t* codes, const float* absmax, float* x, int64_t n,
+                              int kind, const DevTables* tab, cudaStream_t st);
+cudaError_t launch_philox_fill(uint64_t seed, uint32_t step, uint32_t stream_id, uint64_t offset,
+                               int64_t n, uint16_t* out, cudaStream_t st);
+
+}  // namespace q8

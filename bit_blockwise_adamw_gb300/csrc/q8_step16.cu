@@ -1,0 +1,109 @@
+// q8_step16.cu -- BF16-state AdamW with stochastic rounding ("Stochastic
+// Rounding for LLM Training: Theory and Practice", TL;DR: BF16-AdamW-SR;
+// "[Feat]: Stochastic rounding of AdamW momentums": fp32 maths with a
+// stochastically rounded write-back of both momentums).
+//
+// Pure streaming: 8 bytes read and 6 written per element.  A persistent grid
+// walks contiguous ranges of 2048-element blocks; each thread owns eight
+// contiguous elements and draws three independent Philox streams (p, m, v).
+#include "q8_device.cuh"
+
+namespace q8 {
+
+namespace {
+
+__device__ __forceinline__ int find_tensor16(const int32_t* start, int nt, int gb)
+{
+    int lo = 0, hi = nt;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (start[mid] <= gb) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ void load8_bf16(const uint16_t* src, int64_t rem, uint32_t w[4])
+{
+    if (rem >= kVec) {
+        const uint4 q = ld_stream16(src);
+        w[0] = q.x; w[1] = q.y; w[2] = q.z; w[3] = q.w;
+    } else {
+        w[0] = w[1] = w[2] = w[3] = 0;
+        for (int j = 0; j < kVec; ++j)
+            if (j < rem) w[j >> 1] |= static_cast<uint32_t>(src[j]) << ((j & 1) * 16);
+    }
+}
+
+__device__ __forceinline__ void store8_bf16(uint16_t* dst, int64_t rem, const uint32_t w[4])
+{
+    if (rem >= kVec) {
+        st_stream16(dst, make_uint4(w[0], w[1], w[2], w[3]));
+    } else {
+        for (int j = 0; j < kVec; ++j)
+            if (j < rem) dst[j] = static_cast<uint16_t>(w[j >> 1] >> ((j & 1) * 16));
+    }
+}
+
+__global__ void __launch_bounds__(kThreads, 4) step16_kernel(const __grid_constant__ Step16Args a)
+{
+    const Scalars& s = a.s;
+    const bool sr = s.sr != 0;
+    const int begin = static_cast<int>((static_cast<int64_t>(blockIdx.x) * a.nblocks) / gridDim.x);
+    const int end = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * a.nblocks) / gridDim.x);
+    int ti = begin < end ? find_tensor16(a.blk_start, a.nt, begin) : 0;
+
+    for (int gb = begin; gb < end; ++gb) {
+        while (gb >= a.blk_start[ti + 1]) ++ti;
+        const Desc16& d = a.d[ti];
+        const int lb = gb - a.blk_start[ti];
+        const int64_t i0 = static_cast<int64_t>(lb) * kBlock + threadIdx.x * kVec;
+        const int64_t rem = d.n - i0;
+        if (rem <= 0) continue;
+
+        uint32_t gw[4], pw[4], mw[4], vw[4];
+        load8_bf16(d.g + i0, rem, gw);
+        load8_bf16(d.p + i0, rem, pw);
+        load8_bf16(d.m + i0, rem, mw);
+        load8_bf16(d.v + i0, rem, vw);
+
+        float pn[kVec], mn[kVec], vn[kVec];
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const bool hi = j & 1;
+            const uint32_t k = j >> 1;
+            float m = hi ? bf16hi(mw[k]) : bf16lo(mw[k]);
+            float v = hi ? bf16hi(vw[k]) : bf16lo(vw[k]);
+            const float g = hi ? bf16hi(gw[k]) : bf16lo(gw[k]);
+            const float p = hi ? bf16hi(pw[k]) : bf16lo(pw[k]);
+            pn[j] = adamw(s, g, p, m, v);
+            mn[j] = m;
+            vn[j] = v;
+        }
+
+        const uint64_t E = d.e0 + static_cast<uint64_t>(i0);
+        uint32_t r[4] = {0, 0, 0, 0}, out[4];
+        if (sr) draws8(E, 0u, s, r);
+        round8(pn, r, sr, out);
+        store8_bf16(d.p + i0, rem, out);
+        if (sr) draws8(E, 1u, s, r);
+        round8(mn, r, sr, out);
+        store8_bf16(d.m + i0, rem, out);
+        if (sr) draws8(E, 2u, s, r);
+        round8(vn, r, sr, out);
+        store8_bf16(d.v + i0, rem, out);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_step16(const Step16Args& a, cudaStream_t st)
+{
+    static int full = 0;
+    if (full == 0) full = resident_ctas(reinterpret_cast<const void*>(step16_kernel), kThreads, 0);
+    if (full <= 0) return cudaErrorUnknown;
+    const int grid = a.nblocks < full ? a.nblocks : full;
+    if (grid > 0) step16_kernel<<<grid, kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace q8

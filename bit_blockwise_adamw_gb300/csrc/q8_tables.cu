@@ -1,0 +1,148 @@
+// q8_tables.cu -- codebooks, decision midpoints and the cell search table:
+// built once on the host, uploaded once per device.
+//
+// Codebooks ("8-bit Optimizers via Block-wise Quantization", innovations list:
+// dynamic tree quantization, extended to unipolar data).  Reading: after the
+// sign, a run of e zero bits selects the decade 10^-e, an indicator bit
+// follows, and the remaining f bits place the value linearly inside the
+// decade at 10^-e * (0.1 + 0.9*(j+1)/2^f), j = 0..2^f-1.  Signed book: 7 bits
+// after the sign (e = 0..6, f = 6-e), mirrored around zero, with a duplicate
+// 1.0 at index 255 that the search never returns; unsigned book: 8 bits
+// (e = 0..7, f = 7-e) and zero.  Listing the decades from the smallest
+// (largest e) up gives the tables in ascending order directly.
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "q8_internal.h"
+
+namespace q8 {
+
+namespace {
+
+// One decade's values, ascending, appended at out[pos...]; returns new pos.
+int append_decade(int e, int f, float* out, int pos)
+{
+    int64_t scale = 10;
+    for (int i = 0; i < e; ++i) scale *= 10;            // 10^(e+1)
+    const int64_t den = scale << f;                      // 10^(e+1) * 2^f
+    for (int j = 0; j < (1 << f); ++j) {
+        const int64_t num = (int64_t(1) << f) + 9 * int64_t(j + 1);
+        out[pos++] = static_cast<float>(static_cast<double>(num) / static_cast<double>(den));
+    }
+    return pos;
+}
+
+void build_midpoints(const float c[256], float mid[255])
+{
+    for (int j = 0; j < 255; ++j)
+        mid[j] = static_cast<float>(0.5 * (static_cast<double>(c[j]) + static_cast<double>(c[j + 1])));
+}
+
+float bits_to_float(uint32_t u) { float f; std::memcpy(&f, &u, 4); return f; }
+uint32_t float_to_bits(float f) { uint32_t u; std::memcpy(&u, &f, 4); return u; }
+
+// Fill one half (sign s) of a cell table; returns false if a cell would hold
+// more than one midpoint (the table could not then decide with one compare).
+bool build_cells(const float mid[255], int L, int ncells, int sign, uint32_t* out)
+{
+    const uint32_t low = static_cast<uint32_t>(127 - L) << 23;
+    for (int c = 0; c < ncells; ++c) {
+        uint32_t a_lo, a_hi;                              // magnitude bit range
+        if (c == 0) { a_lo = 0; a_hi = low - 1; }
+        else {
+            a_lo = low + (static_cast<uint32_t>(c - 1) << kCellShift);
+            a_hi = a_lo + ((1u << kCellShift) - 1);
+        }
+        if (a_hi > 0x3F800000u) a_hi = 0x3F800000u;
+        if (a_lo > a_hi) a_lo = a_hi;
+        const float x_first = sign ? -bits_to_float(a_hi) : bits_to_float(a_lo);
+        const float x_last = sign ? -bits_to_float(a_lo) : bits_to_float(a_hi);
+        uint32_t base = 0;
+        while (base < 255 && mid[base] < x_first) ++base;
+        int inside = 0;
+        uint32_t ml = 0xFFFFu;
+        for (int j = static_cast<int>(base); j < 255 && mid[j] <= x_last; ++j) {
+            ++inside;
+            const uint32_t low16 = float_to_bits(std::fabs(mid[j])) & 0xFFFFu;
+            ml = sign ? (~low16 & 0xFFFFu) : low16;
+        }
+        if (inside > 1 || (c == 0 && inside > 0)) return false;
+        out[c] = (ml << 16) | base;
+    }
+    return true;
+}
+
+struct HostTables {
+    DevTables t;
+    bool ok = false;
+    HostTables()
+    {
+        float mid_s[255], mid_u[255];
+        build_codebook(Q8_SIGNED, t.cs);
+        build_codebook(Q8_UNSIGNED, t.cu);
+        build_midpoints(t.cs, mid_s);
+        build_midpoints(t.cu, mid_u);
+        ok = build_cells(mid_s, kSignedL, kCellsSigned, 0, t.cell_s)
+          && build_cells(mid_s, kSignedL, kCellsSigned, 1, t.cell_s + kCellsSigned)
+          && build_cells(mid_u, kUnsignedL, kCellsUnsigned, 0, t.cell_u);
+    }
+};
+
+const HostTables& host_tables()
+{
+    static const HostTables h;
+    return h;
+}
+
+__device__ DevTables g_tables;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mutex;
+const DevTables* g_dev_ptr[kMaxDevices] = {};
+
+}  // namespace
+
+void build_codebook(int kind, float out[256])
+{
+    if (kind == Q8_UNSIGNED) {
+        int pos = 0;
+        out[pos++] = 0.0f;
+        for (int e = 7; e >= 0; --e) pos = append_decade(e, 7 - e, out, pos);
+    } else {
+        float mag[127];
+        int pos = 0;
+        for (int e = 6; e >= 0; --e) pos = append_decade(e, 6 - e, mag, pos);
+        for (int i = 0; i < 127; ++i) {
+            out[128 + i] = mag[i];
+            out[126 - i] = -mag[i];
+        }
+        out[127] = 0.0f;
+        out[255] = 1.0f;
+    }
+}
+
+cudaError_t device_tables(const DevTables** out)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (!g_dev_ptr[dev]) {
+        const HostTables& h = host_tables();
+        if (!h.ok) return cudaErrorInvalidValue;
+        err = cudaMemcpyToSymbol(g_tables, &h.t, sizeof(DevTables));
+        if (err != cudaSuccess) return err;
+        err = cudaDeviceSynchronize();
+        if (err != cudaSuccess) return err;
+        void* p = nullptr;
+        err = cudaGetSymbolAddress(&p, g_tables);
+        if (err != cudaSuccess) return err;
+        g_dev_ptr[dev] = static_cast<const DevTables*>(p);
+    }
+    *out = g_dev_ptr[dev];
+    return cudaSuccess;
+}
+
+}  // namespace q8

@@ -1,0 +1,203 @@
+/*
+ * q8adamw.h -- C ABI of the GB300 (sm_103a) fused 8-bit blockwise AdamW step
+ * with stochastic rounding of BF16 parameters, and its BF16-state variant.
+ *
+ * Sources, by page title and section:
+ *  [BW]  "8-bit Optimizers via Block-wise Quantization": innovations list
+ *        (dynamic tree quantization, extended to unipolar data) and method
+ *        bullets (2048-element blocks normalised by their absmax, binary
+ *        search to an 8-bit index, lookup-table dequantization, states
+ *        dequantized, updated in 32 bit and requantized in registers).
+ *  [SR]  "Stochastic rounding support for 8-bit optimizers": feature request
+ *        (stochastic rounding of BF16 parameter updates, no FP32 master
+ *        weights) and scoping comment (FP32-state fallback for small tensors,
+ *        stream compatibility).
+ *  [MOM] "[Feat]: Stochastic rounding of AdamW momentums": state_dtype choice,
+ *        fp32 maths with stochastically rounded write-back of the momentums.
+ *  [LLM] "Stochastic Rounding for LLM Training: Theory and Practice": TL;DR
+ *        (BF16-AdamW-SR; shared randomness across replicas).
+ *
+ * Conventions for every entry point:
+ *  - Pointers named "device" are CUDA device (or managed/host-mapped) memory
+ *    owned by the caller; the library never frees or keeps them.  BF16 values
+ *    are passed as their 16-bit patterns (uint16_t).
+ *  - Work is enqueued asynchronously on `stream` (a cudaStream_t; NULL is the
+ *    legacy default stream).  Nothing synchronises with the host except the
+ *    one-time per-device set-up described at q8_prepare_device().
+ *  - Return value: Q8_OK (0), or a negative q8_status.  Argument errors are
+ *    detected on the host before anything is launched, and leave all buffers
+ *    untouched.  Q8_ERR_CUDA reports a launch or set-up failure.  Faults in
+ *    kernels that already ran surface at the caller's next synchronisation.
+ *    q8_last_error() returns a message for the last failure on the calling
+ *    host thread.
+ *  - Non-finite gradients or states give unspecified values (never a fault).
+ */
+#ifndef Q8ADAMW_H
+#define Q8ADAMW_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* q8_stream_t;   /* same type as cudaStream_t */
+
+typedef enum {
+    Q8_OK = 0,
+    Q8_ERR_NULL = -1,    /* a required pointer is NULL                         */
+    Q8_ERR_SIZE = -2,    /* a size is negative or beyond a stated limit        */
+    Q8_ERR_ALIGN = -3,   /* a pointer breaks the stated alignment              */
+    Q8_ERR_ARG = -4,     /* a hyper-parameter or enum is out of range          */
+    Q8_ERR_CUDA = -5     /* the CUDA runtime reported an error                 */
+} q8_status;
+
+typedef enum { Q8_SIGNED = 0, Q8_UNSIGNED = 1 } q8_kind;
+
+enum {
+    Q8_BLOCK = 2048,          /* [BW] method bullets: elements per absmax block */
+    Q8_SMALL_NUMEL = 4096,    /* tensors below this keep fp32 state ([SR])      */
+    Q8_MAX_STEP = 0x7FFFFFFF  /* the step counter enters Philox as 32 bits      */
+};
+
+/*
+ * AdamW hyper-parameters and the stochastic-rounding key.
+ *   lr >= 0, 0 <= beta1 < 1, 0 <= beta2 < 1, eps >= 0, weight_decay >= 0 (all
+ *   finite); 1 <= step <= Q8_MAX_STEP (the 1-based step being taken, used for
+ *   bias correction and as the Philox counter word); seed keys Philox; sr = 1
+ *   rounds every BF16 write stochastically, sr = 0 rounds to nearest even.
+ * The step forms, in double, a_t = lr*sqrt(1-beta2^t)/(1-beta1^t),
+ * eps_t = eps*sqrt(1-beta2^t) and decay = 1 - lr*weight_decay, rounds each to
+ * float once, and per element computes in fp32 (each operation rounded):
+ *   m = beta1*m + (1-beta1)*g;  v = beta2*v + (1-beta2)*g*g;
+ *   p = p*decay - a_t * m / (sqrt(v) + eps_t)
+ * which equals textbook AdamW with decoupled weight decay ([LLM] TL;DR).
+ */
+typedef struct {
+    double lr, beta1, beta2, eps, weight_decay;
+    int64_t step;
+    uint64_t seed;
+    int32_t sr;
+} q8_adamw_hparams;
+
+/*
+ * One parameter tensor for adamw8bit_sr_step.  All pointers are device
+ * pointers to contiguous 1-D arrays of `numel` elements, 16-byte aligned.
+ *   param          bf16, read and written in place
+ *   grad           bf16, read only
+ *   philox_offset  global Philox index of element 0; a negative value means
+ *                  "the sum of numel over the tensors before this one in the
+ *                  list" (so one list behaves like one flat tensor)
+ * numel >= 4096 (8-bit state, [BW]): m_codes, v_codes are uint8 indices into
+ *   the signed / unsigned codebooks; m_absmax, v_absmax hold one float per
+ *   2048-element block (ceil(numel/2048) entries, 4-byte aligned).  m32/v32
+ *   are ignored.  An all-zero state (codes anything, absmax 0) is the fresh
+ *   state; canonical zero codes are 127 (m) and 0 (v).
+ * numel < 4096 (fp32 state, [SR] scoping comment): m32, v32 are float arrays
+ *   of numel elements, updated in place; the 8-bit fields are ignored.
+ * numel == 0 tensors are skipped.
+ */
+typedef struct {
+    uint16_t* param;
+    const uint16_t* grad;
+    int64_t numel;
+    int64_t philox_offset;
+    uint8_t* m_codes;
+    uint8_t* v_codes;
+    float* m_absmax;
+    float* v_absmax;
+    float* m32;
+    float* v32;
+} q8_tensor8;
+
+/* One tensor for adamw_bf16_sr_step: param, grad, m, v are bf16 device
+ * arrays of numel elements (16-byte aligned), param/m/v updated in place. */
+typedef struct {
+    uint16_t* param;
+    const uint16_t* grad;
+    uint16_t* m;
+    uint16_t* v;
+    int64_t numel;
+    int64_t philox_offset;
+} q8_tensor16;
+
+/*
+ * The 256-entry codebook of `kind`, ascending, written to the HOST array
+ * out[256] ([BW] innovations list: dynamic tree quantization, signed and
+ * unipolar).  Entry j = 0..2^f-1 of decade e is 10^-e*(0.1 + 0.9*(j+1)/2^f)
+ * rounded to float; signed: decades e = 0..6 with f = 6-e, mirrored, zero at
+ * index 127 and a never-produced duplicate 1.0 at index 255; unsigned:
+ * e = 0..7 with f = 7-e, zero at index 0.  Host only; no GPU needed.
+ */
+int q8_codebook_init(int kind, float* out);
+
+/*
+ * Blockwise quantization of n floats ([BW] method bullets): for each
+ * 2048-element block (the last may be partial) absmax[b] = max |x|; each x is
+ * scaled by the correctly rounded reciprocal of absmax[b], clamped to [-1, 1]
+ * and coded as the number of codebook midpoints strictly below it; an
+ * all-zero block gets the zero code.  x: device float[n] (16-byte aligned);
+ * codes: device uint8[n] (16-byte aligned); absmax: device float[ceil(n/2048)]
+ * (4-byte aligned).  For Q8_UNSIGNED, negative x code to 0.  0 <= n < 2^40.
+ */
+int q8_blockwise_quantize(const float* x, uint8_t* codes, float* absmax, int64_t n,
+                          int kind, q8_stream_t stream);
+
+/*
+ * Blockwise dequantization ([BW] method bullets): x[i] = C[codes[i]] *
+ * absmax[i/2048] with C the codebook of `kind`.  Same layouts as above.
+ */
+int q8_blockwise_dequantize(const uint8_t* codes, const float* absmax, float* x, int64_t n,
+                            int kind, q8_stream_t stream);
+
+/*
+ * Fused 8-bit blockwise AdamW step with stochastic rounding of the BF16
+ * parameters ([BW] method bullets; [SR] feature request), over a list of
+ * `ntensors` tensors (host array).  Per 2048-element block: dequantize m, v,
+ * run the AdamW update above in fp32, take the new block absmax of m and v,
+ * requantize them, and write p rounded to bf16 with the 16-bit Philox draw of
+ * element E = philox_offset + i on stream 0 (see q8_philox_fill).  Tensors
+ * below 4096 elements take the fp32-state path with the same maths.  Blocks
+ * never straddle tensors.  0 <= ntensors; the list may mix both paths.
+ */
+int adamw8bit_sr_step(const q8_tensor8* list, int ntensors, const q8_adamw_hparams* hp,
+                      q8_stream_t stream);
+
+/*
+ * BF16-state AdamW with stochastic rounding ([LLM] BF16-AdamW-SR; [MOM] fp32
+ * maths, stochastically rounded write-back of the momentums): m, v are read
+ * from bf16, the same fp32 update runs, and p, m, v are written back rounded
+ * with Philox streams 0, 1 and 2 respectively.
+ */
+int adamw_bf16_sr_step(const q8_tensor16* list, int ntensors, const q8_adamw_hparams* hp,
+                       q8_stream_t stream);
+
+/*
+ * The 16-bit random draws the steps use, for inspection: out[i] = r16(E) for
+ * E = offset + i, where Philox4x32-10 (Salmon et al., SC'11) with key
+ * (seed & 0xffffffff, seed >> 32) and counter (lo32(E/8), stream_id, step,
+ * hi32(E/8)) yields four words and element E takes the (E & 1) half (0 = low
+ * 16 bits) of word (E >> 1) & 3.  out: device uint16[n] (2-byte aligned).
+ */
+int q8_philox_fill(uint64_t seed, uint32_t step, uint32_t stream_id, uint64_t offset,
+                   int64_t n, uint16_t* out, q8_stream_t stream);
+
+/*
+ * One-time set-up of the current device: uploads the codebooks and search
+ * tables and waits for the copy (a device-wide synchronisation).  Every
+ * other entry point calls it on first use; call it yourself before capturing
+ * a CUDA graph or when the first step must not synchronise.
+ */
+int q8_prepare_device(void);
+
+/* Message for the last failure on this host thread ("" if none). */
+const char* q8_last_error(void);
+
+/* ABI version: bumped on any change of a signature or struct. */
+int q8_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q8ADAMW_H */

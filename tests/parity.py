@@ -1,0 +1,219 @@
+"""Helpers shared by the GPU parity tests: run the CUDA path through the
+binding, replay the same inputs through the oracle, compare element by
+element.  Inputs come from bit_blockwise_adamw_gb300.workloads (seeded torch
+generators); no expected value is taken from the CUDA path."""
+import multiprocessing as mp
+
+import numpy as np
+import torch
+
+import bit_blockwise_adamw_gb300 as q8
+from bit_blockwise_adamw_gb300 import workloads as W
+import oracle as o
+
+BLOCK = 2048
+
+
+def u16(t: torch.Tensor) -> np.ndarray:
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def hp_for(wl, step, sr=1):
+    h = wl.hp
+    return dict(lr=h["lr"], beta1=h["beta1"], beta2=h["beta2"], eps=h["eps"],
+                weight_decay=h["weight_decay"], step=step, seed=wl.philox_seed, sr=sr)
+
+
+def gpu_states8(params, offsets=None):
+    offsets = offsets or [-1] * len(params)
+    return [q8.Tensor8.zeros_like(p, None, philox_offset=off) for p, off in zip(params, offsets)]
+
+
+def host_states8(params_host, offsets=None):
+    offsets = offsets or [-1] * len(params_host)
+    return [o.State8.zeros(p.copy(), np.zeros_like(p), philox_offset=off)
+            for p, off in zip(params_host, offsets)]
+
+
+def compare_state8(gpu, host, where=""):
+    """Bit-exact comparison of one tensor's parameters and state."""
+    np.testing.assert_array_equal(u16(gpu.param), host.param, err_msg="param " + where)
+    if host.m_codes is not None:
+        np.testing.assert_array_equal(gpu.m_codes.cpu().numpy(), host.m_codes, err_msg="m codes " + where)
+        np.testing.assert_array_equal(gpu.v_codes.cpu().numpy(), host.v_codes, err_msg="v codes " + where)
+        np.testing.assert_array_equal(gpu.m_absmax.cpu().numpy().view(np.uint32),
+                                      host.m_absmax.view(np.uint32), err_msg="m absmax " + where)
+        np.testing.assert_array_equal(gpu.v_absmax.cpu().numpy().view(np.uint32),
+                                      host.v_absmax.view(np.uint32), err_msg="v absmax " + where)
+    else:
+        np.testing.assert_array_equal(gpu.m32.cpu().numpy().view(np.uint32), host.m32.view(np.uint32),
+                                      err_msg="m32 " + where)
+        np.testing.assert_array_equal(gpu.v32.cpu().numpy().view(np.uint32), host.v32.view(np.uint32),
+                                      err_msg="v32 " + where)
+
+
+# ---------------------------------------------------------------- sampled replay
+# Each 2048-block's trajectory depends only on its own inputs, so the oracle
+# can replay any chosen blocks over all steps.  Workers are started with
+# "spawn" (a forked child of a CUDA process can hang).
+
+def _replay8(job):
+    """Oracle replay of one 8-bit block: job = (param0, grads[steps], E0, hps)."""
+    p0, grads, e0, hps = job
+    st = o.State8(p0.copy(), grads[0], np.full(p0.size, o.zero_code(o.SIGNED), np.uint8),
+                  np.full(p0.size, o.zero_code(o.UNSIGNED), np.uint8),
+                  np.zeros(1, np.float32), np.zeros(1, np.float32))
+    for g, h in zip(grads, hps):
+        st.grad = g
+        o.adamw8bit_tensor(st, e0, o.hparams(**h))
+    return st.param, st.m_codes, st.v_codes, st.m_absmax, st.v_absmax
+
+
+def _replay32(job):
+    p0, grads, e0, hps = job
+    n = p0.size
+    st = o.State8(p0.copy(), grads[0], m32=np.zeros(n, np.float32), v32=np.zeros(n, np.float32))
+    for g, h in zip(grads, hps):
+        st.grad = g
+        o.adamw32_tensor(st, e0, o.hparams(**h))
+    return st.param, st.m32, st.v32
+
+
+def _replay16(job):
+    p0, grads, e0, hps = job
+    n = p0.size
+    st = o.State16(p0.copy(), grads[0], np.zeros(n, np.uint16), np.zeros(n, np.uint16))
+    for g, h in zip(grads, hps):
+        st.grad = g
+        o.adamw_bf16_tensor(st, e0, o.hparams(**h))
+    return st.param, st.m, st.v
+
+
+def oracle_pool(processes=None):
+    return mp.get_context("spawn").Pool(processes)
+
+
+class SampledRun:
+    """Run a full-size workload on the GPU while recording the inputs of the
+    sampled blocks (and of every small tensor) for an oracle replay."""
+
+    def __init__(self, wl, device, fraction, steps=None):
+        self.wl = wl
+        self.steps = steps or wl.steps
+        self.device = device
+        self.picks = W.sample_blocks(wl, fraction)
+        self.small = wl.small_tensors() if wl.state == "8bit" else []
+        self.offsets = W.philox_offsets(wl)
+        self.by_tensor = {}
+        for i, b in self.picks:
+            self.by_tensor.setdefault(i, []).append(b)
+
+    def _gather(self, tensors, conv):
+        """Host copies of the sampled blocks of per-element tensors, batched
+        into one gather and one copy per tensor."""
+        out = {}
+        for i, blocks in self.by_tensor.items():
+            t = tensors[i]
+            nfull = t.numel() // BLOCK
+            full = [b for b in blocks if b < nfull]
+            if full:
+                idx = torch.tensor(full, device=t.device)
+                rows = conv(t[:nfull * BLOCK].view(nfull, BLOCK)[idx])
+                for j, b in enumerate(full):
+                    out[(i, b)] = rows[j]
+            for b in blocks:
+                if b >= nfull:
+                    out[(i, b)] = conv(t[b * BLOCK:])
+        return out
+
+    def _slices(self, tensors):
+        out = self._gather(tensors, u16)
+        for i in self.small:
+            out[(i, -1)] = u16(tensors[i])
+        return out
+
+    def run(self):
+        wl, dev = self.wl, self.device
+        params = W.init_params(wl, dev)
+        self.p0 = self._slices(params)
+        self.grads = []
+        self.hps = []
+        if wl.state == "8bit":
+            states = gpu_states8(params)
+        else:
+            states = [q8.Tensor16(p, None, torch.zeros_like(p), torch.zeros_like(p)) for p in params]
+        packed = None
+        for step in range(1, self.steps + 1):
+            grads = W.make_grads(wl, step, dev)
+            for s, g in zip(states, grads):
+                s.grad = g
+            packed = q8.pack_tensor8(states) if wl.state == "8bit" else q8.pack_tensor16(states)
+            h = hp_for(wl, step)
+            if wl.state == "8bit":
+                q8.adamw8bit_sr_step(packed, q8.hparams(**h))
+            else:
+                q8.adamw_bf16_sr_step(packed, q8.hparams(**h))
+            self.grads.append(self._slices(grads))
+            self.hps.append(h)
+            del grads
+        torch.cuda.synchronize()
+        self.final = {}
+        npy = lambda t: t.cpu().numpy()
+        fp = self._gather([s.param for s in states], u16)
+        if wl.state == "8bit":
+            fm = self._gather([s.m_codes if s.m_codes is not None else s.param for s in states], npy)
+            fv = self._gather([s.v_codes if s.v_codes is not None else s.param for s in states], npy)
+            for i, b in self.picks:
+                s = states[i]
+                self.final[(i, b)] = (fp[(i, b)], fm[(i, b)], fv[(i, b)],
+                                      npy(s.m_absmax[b:b + 1]), npy(s.v_absmax[b:b + 1]))
+        else:
+            fm = self._gather([s.m for s in states], u16)
+            fv = self._gather([s.v for s in states], u16)
+            for k in self.picks:
+                self.final[k] = (fp[k], fm[k], fv[k])
+        for i in self.small:
+            s = states[i]
+            self.final[(i, -1)] = (u16(s.param), s.m32.cpu().numpy(), s.v32.cpu().numpy())
+        del states, params
+        torch.cuda.empty_cache()
+
+    def jobs(self):
+        keys = list(self.picks) + [(i, -1) for i in self.small]
+        out = []
+        for k in keys:
+            i, b = k
+            e0 = self.offsets[i] + (b * BLOCK if b >= 0 else 0)
+            out.append((k, (self.p0[k], [g[k] for g in self.grads], e0, self.hps)))
+        return out
+
+    def check(self, pool):
+        """Replay every sampled block on the oracle; return the number of
+        elements compared.  Raises on the first mismatch."""
+        jobs = self.jobs()
+        fns = []
+        for k, job in jobs:
+            if k[1] == -1:
+                fns.append(_replay32)
+            elif self.wl.state == "8bit":
+                fns.append(_replay8)
+            else:
+                fns.append(_replay16)
+        results = [pool.apply_async(f, (job,)) for f, (_, job) in zip(fns, jobs)]
+        compared = 0
+        for (k, _), r in zip(jobs, results):
+            want = r.get()
+            got = self.final[k]
+            names = ("param", "m", "v", "m_absmax", "v_absmax")
+            for name, gv, wv in zip(names, got, want):
+                gv = np.asarray(gv)
+                wv = np.asarray(wv)
+                if gv.dtype == np.float32:
+                    gv, wv = gv.view(np.uint32), wv.view(np.uint32)
+                if not np.array_equal(gv, wv):
+                    bad = np.nonzero(gv != wv)[0]
+                    raise AssertionError("%s mismatch in tensor %d block %d: %d of %d differ, first at %d "
+                                         "(gpu %r oracle %r)" % (name, k[0], k[1], bad.size, gv.size,
+                                                                  bad[0], gv[bad[0]], wv[bad[0]]))
+            compared += got[0].size
+        return compared

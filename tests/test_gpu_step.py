@@ -1,0 +1,185 @@
+"""GPU parity of the fused steps against the oracle, through the C ABI.
+
+Small cases compare every element after every step; the full-size workloads
+(the model-shaped tensor lists at their real sizes, launched exactly as the
+benchmark launches them) compare a seeded sample of 2048-blocks, every small
+tensor and the first and last block of every tensor, replayed by the oracle
+over all steps.  The bar is bit-exact parameters, codes, absmax and fp32
+state (the method has one correct answer once its readings are fixed).
+"""
+import numpy as np
+import pytest
+import torch
+
+import bit_blockwise_adamw_gb300 as q8
+from bit_blockwise_adamw_gb300 import workloads as W
+import oracle as o
+
+from parity import (SampledRun, compare_state8, gpu_states8, host_states8, hp_for, oracle_pool, u16)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pool():
+    p = oracle_pool()
+    yield p
+    p.close()
+    p.join()
+
+
+def _run_full(wl, device, steps=None, sr=1, offsets=None, split=None):
+    """Run `wl` on both sides for `steps`, comparing everything after each step."""
+    steps = steps or wl.steps
+    params = W.init_params(wl, device)
+    gpu = gpu_states8(params, offsets)
+    host = host_states8([u16(p) for p in params], offsets)
+    for step in range(1, steps + 1):
+        grads = W.make_grads(wl, step, device)
+        for g_gpu, g_host, gr in zip(gpu, host, grads):
+            g_gpu.grad = gr
+            g_host.grad = u16(gr)
+        h = hp_for(wl, step, sr)
+        if split:
+            q8.adamw8bit_sr_step(gpu[:split], q8.hparams(**h))
+            q8.adamw8bit_sr_step(gpu[split:], q8.hparams(**h))
+        else:
+            q8.adamw8bit_sr_step(gpu, q8.hparams(**h))
+        o.adamw8bit_sr_step(host, o.hparams(**h))
+        torch.cuda.synchronize()
+        for i, (a, b) in enumerate(zip(gpu, host)):
+            compare_state8(a, b, "tensor %d step %d" % (i, step))
+    return gpu, host
+
+
+def test_flat_1m_full_parity(cuda_device):
+    """1,048,576 params, 512 blocks, 10 steps, every element every step."""
+    _run_full(W.WORKLOADS["flat-1m"], cuda_device)
+
+
+EDGE_SIZES = [1, 7, 8, 9, 2047, 2048, 4095, 4096, 4097, 3 * 2048 + 1, 12345, 65536 + 24, 0, 300]
+
+
+@pytest.mark.parametrize("sr", [1, 0])
+def test_edge_sizes_mixed_paths(cuda_device, sr):
+    """Ragged tails, partial blocks, the 4095/4096 routing edge and an empty
+    tensor in one list, 4 steps, both rounding modes."""
+    wl = W.custom("edges", EDGE_SIZES, steps=4, outlier_rate=0.01, outlier_factor=50.0, data_seed=77)
+    _run_full(wl, cuda_device, sr=sr)
+
+
+def test_explicit_misaligned_offsets(cuda_device):
+    """Philox offsets that are not multiples of 8 (draws span two counters)."""
+    sizes = [5000, 4099, 700, 2048 * 5 + 3]
+    wl = W.custom("offsets", sizes, steps=3, data_seed=78)
+    _run_full(wl, cuda_device, offsets=[3, 1 << 33, 12345677, 7])
+
+
+def test_split_list_equals_whole_list(cuda_device):
+    """Splitting a list with explicit global offsets gives the same bits as one call."""
+    sizes = [8192, 3000, 2048 * 7 + 11, 4096]
+    wl = W.custom("split", sizes, steps=3, data_seed=79)
+    offs = W.philox_offsets(wl)
+    a, _ = _run_full(wl, cuda_device)
+    b, _ = _run_full(wl, cuda_device, offsets=offs, split=2)
+    for x, y in zip(a, b):
+        assert torch.equal(x.param, y.param)
+
+
+def test_resume_equals_continuous(cuda_device):
+    """5 + 5 steps with the state round-tripped through host memory equals 10 steps."""
+    wl = W.custom("resume", [2048 * 9 + 5, 1000], steps=10, data_seed=80)
+    params = W.init_params(wl, cuda_device)
+    ref = gpu_states8([p.clone() for p in params])
+    res = gpu_states8([p.clone() for p in params])
+    for step in range(1, 11):
+        grads = W.make_grads(wl, step, cuda_device)
+        h = q8.hparams(**hp_for(wl, step))
+        for s, g in zip(ref, grads):
+            s.grad = g
+        q8.adamw8bit_sr_step(ref, h)
+        for s, g in zip(res, grads):
+            s.grad = g
+        q8.adamw8bit_sr_step(res, h)
+        if step == 5:   # checkpoint: copy everything to the host and back
+            for s in res:
+                for f in ("param", "m_codes", "v_codes", "m_absmax", "v_absmax", "m32", "v32"):
+                    t = getattr(s, f)
+                    if t is not None:
+                        t.copy_(t.cpu().to(cuda_device))
+    torch.cuda.synchronize()
+    for a, b in zip(ref, res):
+        assert torch.equal(a.param, b.param)
+
+
+def test_many_tensors_take_several_launches(cuda_device):
+    """More tensors than one launch carries (448 per launch)."""
+    sizes = [4096 + 8 * (i % 5) for i in range(500)] + [100 + i for i in range(460)]
+    wl = W.custom("many", sizes, steps=2, data_seed=81)
+    _run_full(wl, cuda_device)
+
+
+def _run_bf16(wl, device, steps, offsets=None, sr=1):
+    params = W.init_params(wl, device)
+    offsets = offsets or [-1] * len(params)
+    gpu = [q8.Tensor16(p, None, torch.zeros_like(p), torch.zeros_like(p), off) for p, off in zip(params, offsets)]
+    host = [o.State16(u16(p), np.zeros(p.numel(), np.uint16), np.zeros(p.numel(), np.uint16),
+                      np.zeros(p.numel(), np.uint16), off) for p, off in zip(params, offsets)]
+    for step in range(1, steps + 1):
+        grads = W.make_grads(wl, step, device)
+        for a, b, g in zip(gpu, host, grads):
+            a.grad = g
+            b.grad = u16(g)
+        h = hp_for(wl, step, sr)
+        q8.adamw_bf16_sr_step(gpu, q8.hparams(**h))
+        o.adamw_bf16_sr_step(host, o.hparams(**h))
+        torch.cuda.synchronize()
+        for i, (a, b) in enumerate(zip(gpu, host)):
+            for name, x, y in (("param", a.param, b.param), ("m", a.m, b.m), ("v", a.v, b.v)):
+                np.testing.assert_array_equal(u16(x), y, err_msg="%s tensor %d step %d" % (name, i, step))
+
+
+@pytest.mark.parametrize("sr", [1, 0])
+def test_bf16_state_full_parity(cuda_device, sr):
+    wl = W.custom("bf16", [1, 7, 2048, 2049, 5000, 1 << 18, 0, 333], steps=5, data_seed=82,
+                  hp=dict(lr=1.2e-3, weight_decay=0.1), grad_std=1e-4)
+    _run_bf16(wl, cuda_device, 5, sr=sr)
+
+
+def test_bf16_state_misaligned_offsets(cuda_device):
+    wl = W.custom("bf16off", [1000, 4099, 2048 * 3 + 5], steps=3, data_seed=83)
+    _run_bf16(wl, cuda_device, 3, offsets=[5, (1 << 34) + 1, 77])
+
+
+def test_empty_list_and_zero_tensor(cuda_device):
+    q8.adamw8bit_sr_step([], q8.hparams())
+    q8.adamw_bf16_sr_step([], q8.hparams())
+    p = torch.zeros(0, dtype=torch.bfloat16, device=cuda_device)
+    q8.adamw8bit_sr_step([q8.Tensor8(p, p, m32=torch.zeros(0, device=cuda_device),
+                                     v32=torch.zeros(0, device=cuda_device))], q8.hparams())
+    torch.cuda.synchronize()
+
+
+def test_bad_arguments_raise(cuda_device):
+    p = torch.zeros(8192, dtype=torch.bfloat16, device=cuda_device)
+    st = q8.Tensor8.zeros_like(p, p.clone())
+    with pytest.raises(q8.Q8Error):
+        q8.adamw8bit_sr_step([st], q8.hparams(step=0))
+    st.param = p[1:4097]                       # misaligned view
+    st.grad = p[1:4097]
+    with pytest.raises(q8.Q8Error):
+        q8.adamw8bit_sr_step([st], q8.hparams())
+
+
+# ---------------------------------------------------------------- full size
+
+FULL = [("gpt2-350m", 0.01), ("gpt2-xl-1.5b", 0.005), ("gptneo-6.7b", 0.003), ("gptneo-2.7b-bf16", 0.003)]
+
+
+@pytest.mark.parametrize("name,fraction", FULL)
+def test_full_size_sampled_parity(cuda_device, pool, name, fraction):
+    wl = W.WORKLOADS[name]
+    run = SampledRun(wl, cuda_device, fraction)
+    run.run()
+    compared = run.check(pool)
+    assert compared > 0
