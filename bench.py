@@ -184,7 +184,7 @@ def oracle_sample_time(wl, nblocks, seed=0):
         states = [o.State16(p[k].copy(), g[k].copy(), np.zeros(BLOCK, np.uint16), np.zeros(BLOCK, np.uint16))
                   for k in range(nblocks)]
     else:
-        states = [o.State8.zeros(p[k].copy(), g[k].copy()) for k in range(nblocks)]
+        states = [o.State8.zeros(p[k].copy(), g[k].copy(), eight_bit=True) for k in range(nblocks)]
     e0 = [offs[bigs[pick[k]]] for k in range(nblocks)]
     t0 = time.perf_counter()
     for k, s in enumerate(states):

@@ -194,9 +194,12 @@ class State8:
         self.philox_offset = philox_offset
 
     @classmethod
-    def zeros(cls, param, grad, philox_offset=-1):
+    def zeros(cls, param, grad, philox_offset=-1, eight_bit=None):
+        """Fresh state; the 8-bit layout when eight_bit (default: numel >= 4096)."""
         n = param.size
-        if n >= SMALL:
+        if eight_bit is None:
+            eight_bit = n >= SMALL
+        if eight_bit:
             nb = (n + BLOCK - 1) // BLOCK
             return cls(param, grad, np.full(n, zero_code(SIGNED), np.uint8),
                        np.full(n, zero_code(UNSIGNED), np.uint8),
@@ -234,11 +237,17 @@ def adamw8bit_sr_step(states, hp):
 
 def adamw8bit_tensor(state, E0, hp):
     """8-bit path on one tensor (or a block-aligned slice) with explicit offset."""
+    if state.m_codes is None or state.v_codes is None or state.m_absmax is None or state.v_absmax is None:
+        raise ValueError("adamw8bit_tensor needs the 8-bit state arrays")
+    if state.m_absmax.size < (state.param.size + BLOCK - 1) // BLOCK:
+        raise ValueError("absmax arrays are too short")
     t = state.struct()
     lib().q8o_adamw8bit_tensor(C.byref(t), E0, C.byref(hp))
 
 
 def adamw32_tensor(state, E0, hp):
+    if state.m32 is None or state.v32 is None:
+        raise ValueError("adamw32_tensor needs m32 and v32")
     t = state.struct()
     lib().q8o_adamw32_tensor(C.byref(t), E0, C.byref(hp))
 
