@@ -14,7 +14,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const float* __restr
                                                             float* __restrict__ absmax, int64_t n,
                                                             int64_t nblocks, const DevTables* tab)
 {
-    constexpr int kCells = KIND == Q8_SIGNED ? 2 * kCellsSigned : kCellsUnsigned;
+    constexpr int kCells = KIND == Q8_SIGNED ? kCellSEntries : kCellsUnsigned;
     __shared__ uint32_t s_cell[kCells];
     __shared__ float s_red[2][kWarps];
     const uint32_t* src = KIND == Q8_SIGNED ? tab->cell_s : tab->cell_u;
@@ -40,7 +40,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const float* __restr
         float lm = 0.0f;
 #pragma unroll
         for (int j = 0; j < kVec; ++j) lm = fmaxf(lm, fabsf(xv[j]));
-        lm = warp_max(lm);
+        lm = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, __float_as_uint(lm)));   // lm >= 0
         if (lane == 0) s_red[it & 1][warp] = lm;
         __syncthreads();
         float M = 0.0f;
@@ -56,7 +56,7 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const float* __restr
             const uint32_t c = M > 0.0f ? (KIND == Q8_SIGNED ? code_signed(y, s_cell)
                                                              : code_unsigned(y, s_cell))
                                         : kZero;
-            q[j >> 2] |= c << ((j & 3) * 8);
+            q[j >> 2] |= (c & 0xFFu) << ((j & 3) * 8);
         }
         if (rem >= kVec) {
             st_stream8(codes + i0, make_uint2(q[0], q[1]));

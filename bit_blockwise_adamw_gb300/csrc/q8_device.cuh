@@ -1,6 +1,7 @@
 // q8_device.cuh -- device-side building blocks of the step kernels: bf16 bit
 // conversions, Philox4x32-10, stochastic rounding, the fp32 AdamW element
-// update and the cell-table code search.
+// update (on pairs, with Blackwell's packed fp32x2 instructions) and the
+// cell-table code search.
 #pragma once
 
 #include "q8_internal.h"
@@ -10,6 +11,8 @@ namespace q8 {
 // ---------------------------------------------------------------- bf16 bits
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+// The two bf16 values of one word as (low element, high element).
+__device__ __forceinline__ float2 bf16x2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
 
 // ---------------------------------------------------------------- Philox
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of
@@ -68,8 +71,8 @@ __device__ __forceinline__ void draws8(uint64_t E, uint32_t sid, const Scalars& 
 // ---------------------------------------------------------------- rounding
 // Stochastic rounding fp32 -> bf16 ("Stochastic rounding support for 8-bit
 // optimizers", feature request): add a uniform 16-bit draw to the bit pattern
-// and keep the top half; NaN becomes 0x7FC0.  Returns the 32-bit pattern whose
-// top half is the bf16 result (so two results pack with one byte permute).
+// and keep the top half; NaN becomes 0x7FC0.  These return the 32-bit pattern
+// whose top half is the bf16 result, so two results pack with one permute.
 __device__ __forceinline__ uint32_t sr_hi(float x, uint32_t r16)
 {
     const uint32_t u = __float_as_uint(x) + r16;
@@ -85,66 +88,95 @@ __device__ __forceinline__ uint32_t rne_hi(float x)
 // Top halves of a and b -> (b_hi << 16) | a_hi.
 __device__ __forceinline__ uint32_t pack_hi(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x7632); }
 
-// Round eight fp32 values to bf16 and pack them into four words.
-__device__ __forceinline__ void round8(const float x[8], const uint32_t r[4], bool sr, uint32_t out[4])
+// Round a pair to bf16 and pack it into one word (draws in r: low half for
+// the first element, high half for the second).
+template <bool SR>
+__device__ __forceinline__ uint32_t round2(float2 x, uint32_t r)
 {
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-        const uint32_t lo = sr ? sr_hi(x[2 * j], r[j] & 0xFFFFu) : rne_hi(x[2 * j]);
-        const uint32_t hi = sr ? sr_hi(x[2 * j + 1], r[j] >> 16) : rne_hi(x[2 * j + 1]);
-        out[j] = pack_hi(lo, hi);
-    }
+    if constexpr (SR) return pack_hi(sr_hi(x.x, r & 0xFFFFu), sr_hi(x.y, r >> 16));
+    else return pack_hi(rne_hi(x.x), rne_hi(x.y));
 }
 
 // ---------------------------------------------------------------- AdamW
-// One element, fp32, every operation rounded on its own (no contraction):
-//   m = b1*m + (1-b1)*g;  v = b2*v + (1-b2)*g*g;
-//   p = p*decay - a_t * (m / (sqrt(v) + eps_t))
-__device__ __forceinline__ float adamw(const Scalars& s, float g, float p, float& m, float& v)
+// The fp32 update, with each multiply-add fused (one rounding) and every
+// other operation rounded on its own:
+//   m = fma(b1, m, (1-b1)*g);  v = fma(b2, v, (1-b2)*(g*g));
+//   p = fma(-a_t, m / (sqrt(v) + eps_t), p*decay)
+// Pairs use the packed fp32x2 instructions (per lane identical to the scalar
+// _rn operations).  Every product feeds an explicit fma or nothing, so the
+// compiler has no multiply-add left to contract; the square root, the eps add
+// and the division stay scalar.
+__device__ __forceinline__ float2 splat(float x) { return make_float2(x, x); }
+
+__device__ __forceinline__ float2 adamw2(const Scalars& s, float2 g, float2 p, float2& m, float2& v)
 {
-    const float mn = __fadd_rn(__fmul_rn(s.b1, m), __fmul_rn(s.omb1, g));
-    const float vn = __fadd_rn(__fmul_rn(s.b2, v), __fmul_rn(s.omb2, __fmul_rn(g, g)));
-    const float den = __fadd_rn(__fsqrt_rn(vn), s.eps_t);
-    const float ratio = __fdiv_rn(mn, den);
+    const float2 mn = __ffma2_rn(splat(s.b1), m, __fmul2_rn(splat(s.omb1), g));
+    const float2 vn = __ffma2_rn(splat(s.b2), v, __fmul2_rn(splat(s.omb2), __fmul2_rn(g, g)));
+    const float2 ratio = make_float2(__fdiv_rn(mn.x, __fadd_rn(__fsqrt_rn(vn.x), s.eps_t)),
+                                     __fdiv_rn(mn.y, __fadd_rn(__fsqrt_rn(vn.y), s.eps_t)));
     m = mn;
     v = vn;
-    return __fsub_rn(__fmul_rn(p, s.decay), __fmul_rn(s.step_size, ratio));
+    return __ffma2_rn(splat(-s.step_size), ratio, __fmul2_rn(p, splat(s.decay)));
+}
+
+// Scalar form (same rounding), for the small-tensor kernel.
+__device__ __forceinline__ float adamw(const Scalars& s, float g, float p, float& m, float& v)
+{
+    const float mn = __fmaf_rn(s.b1, m, __fmul_rn(s.omb1, g));
+    const float vn = __fmaf_rn(s.b2, v, __fmul_rn(s.omb2, __fmul_rn(g, g)));
+    const float ratio = __fdiv_rn(mn, __fadd_rn(__fsqrt_rn(vn), s.eps_t));
+    m = mn;
+    v = vn;
+    return __fmaf_rn(-s.step_size, ratio, __fmul_rn(p, s.decay));
 }
 
 // ---------------------------------------------------------------- search
 // Code of a normalised value x: the number of codebook midpoints strictly
-// below clamp(x, -1, 1), read from the cell table (see q8_internal.h).
-template <int L, int kCellsPerSign>
-__device__ __forceinline__ uint32_t cell_code(uint32_t u, const uint32_t* cells)
-{
-    const uint32_t a = min(u & 0x7FFFFFFFu, 0x3F800000u);        // |x| clamped to 1
-    const int t = static_cast<int>(a) - ((127 - L) << 23);
-    const int cell = max((t >> kCellShift) + 1, 0);
-    const uint32_t neg = static_cast<uint32_t>(static_cast<int>(u) >> 31);
-    const uint32_t e = cells[cell + (neg & static_cast<uint32_t>(kCellsPerSign))];
-    const uint32_t xs = (a ^ neg) << 16;                          // low 16 bits, complemented if x < 0
-    return (e & 0xFFu) + (xs > e ? 1u : 0u);
-}
-
+// below clamp(x, -1, 1), read from the cell table (layout in q8_internal.h).
+// The result is correct in its low byte; callers pack codes with byte
+// permutes, which ignore the upper bits.
 __device__ __forceinline__ uint32_t code_signed(float x, const uint32_t* cells)
 {
-    return cell_code<kSignedL, kCellsSigned>(__float_as_uint(x), cells);
+    const uint32_t u = __float_as_uint(x);
+    const uint32_t a = min(u & 0x7FFFFFFFu, 0x3F800000u);            // |x| clamped to 1
+    const int cell = __viaddmax_s32(static_cast<int>(a >> kCellShift), kSignedCellBias, 0);
+    const uint32_t neg = static_cast<uint32_t>(static_cast<int>(u) >> 31);
+    const uint32_t e = cells[static_cast<uint32_t>(cell) | (neg & kSignedHalf)];
+    const uint32_t xs = (a ^ neg) << 16;                              // low 16 bits, complemented if x < 0
+    return e + (xs > e ? 1u : 0u);
 }
 
-// Unsigned book: negative x (and -0) code as +0; only the non-negative half
-// of the table exists.
+// Unsigned book, non-negative x only (the second moment is never negative).
+__device__ __forceinline__ uint32_t code_unsigned_nonneg(float x, const uint32_t* cells)
+{
+    const uint32_t a = min(__float_as_uint(x), 0x3F800000u);
+    const int cell = __viaddmax_s32(static_cast<int>(a >> kCellShift), kUnsignedCellBias, 0);
+    const uint32_t e = cells[cell];
+    return e + ((a << 16) > e ? 1u : 0u);
+}
+
+// Unsigned book, any x: negative values (and -0) code as +0.
 __device__ __forceinline__ uint32_t code_unsigned(float x, const uint32_t* cells)
 {
-    const uint32_t u = static_cast<uint32_t>(max(static_cast<int>(__float_as_uint(x)), 0));
-    return cell_code<kUnsignedL, 0>(u, cells);
+    const int u = max(static_cast<int>(__float_as_uint(x)), 0);
+    return code_unsigned_nonneg(__int_as_float(u), cells);
 }
 
-// ---------------------------------------------------------------- misc
-__device__ __forceinline__ float warp_max(float x)
+// Four codes (low bytes of q0..q3) -> one word, q0 in the lowest byte.
+__device__ __forceinline__ uint32_t pack4(uint32_t q0, uint32_t q1, uint32_t q2, uint32_t q3)
 {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) x = fmaxf(x, __shfl_xor_sync(0xFFFFFFFFu, x, o));
-    return x;
+    return __byte_perm(__byte_perm(q0, q1, 0x0040), __byte_perm(q2, q3, 0x0040), 0x5410);
+}
+
+// Byte j (0..3) of w, zero-extended.
+__device__ __forceinline__ uint32_t byte_of(uint32_t w, int j) { return __byte_perm(w, 0u, 0x4440 | j); }
+
+// ---------------------------------------------------------------- misc
+__device__ __forceinline__ float max3(float a, float b, float c)
+{
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
 }
 
 // Streaming loads/stores: every byte of the step is touched once.

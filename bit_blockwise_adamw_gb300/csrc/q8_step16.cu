@@ -44,10 +44,10 @@ __device__ __forceinline__ void store8_bf16(uint16_t* dst, int64_t rem, const ui
     }
 }
 
+template <bool SR>
 __global__ void __launch_bounds__(kThreads, 4) step16_kernel(const __grid_constant__ Step16Args a)
 {
     const Scalars& s = a.s;
-    const bool sr = s.sr != 0;
     const int begin = static_cast<int>((static_cast<int64_t>(blockIdx.x) * a.nblocks) / gridDim.x);
     const int end = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * a.nblocks) / gridDim.x);
     int ti = begin < end ? find_tensor16(a.blk_start, a.nt, begin) : 0;
@@ -66,31 +66,26 @@ __global__ void __launch_bounds__(kThreads, 4) step16_kernel(const __grid_consta
         load8_bf16(d.m + i0, rem, mw);
         load8_bf16(d.v + i0, rem, vw);
 
-        float pn[kVec], mn[kVec], vn[kVec];
-#pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-            const bool hi = j & 1;
-            const uint32_t k = j >> 1;
-            float m = hi ? bf16hi(mw[k]) : bf16lo(mw[k]);
-            float v = hi ? bf16hi(vw[k]) : bf16lo(vw[k]);
-            const float g = hi ? bf16hi(gw[k]) : bf16lo(gw[k]);
-            const float p = hi ? bf16hi(pw[k]) : bf16lo(pw[k]);
-            pn[j] = adamw(s, g, p, m, v);
-            mn[j] = m;
-            vn[j] = v;
-        }
-
         const uint64_t E = d.e0 + static_cast<uint64_t>(i0);
-        uint32_t r[4] = {0, 0, 0, 0}, out[4];
-        if (sr) draws8(E, 0u, s, r);
-        round8(pn, r, sr, out);
-        store8_bf16(d.p + i0, rem, out);
-        if (sr) draws8(E, 1u, s, r);
-        round8(mn, r, sr, out);
-        store8_bf16(d.m + i0, rem, out);
-        if (sr) draws8(E, 2u, s, r);
-        round8(vn, r, sr, out);
-        store8_bf16(d.v + i0, rem, out);
+        uint32_t rp[4] = {0, 0, 0, 0}, rm[4] = {0, 0, 0, 0}, rv[4] = {0, 0, 0, 0};
+        if constexpr (SR) {
+            draws8(E, 0u, s, rp);
+            draws8(E, 1u, s, rm);
+            draws8(E, 2u, s, rv);
+        }
+        uint32_t po[4], mo[4], vo[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            float2 m = bf16x2(mw[k]);
+            float2 v = bf16x2(vw[k]);
+            const float2 pn = adamw2(s, bf16x2(gw[k]), bf16x2(pw[k]), m, v);
+            po[k] = round2<SR>(pn, rp[k]);
+            mo[k] = round2<SR>(m, rm[k]);
+            vo[k] = round2<SR>(v, rv[k]);
+        }
+        store8_bf16(d.p + i0, rem, po);
+        store8_bf16(d.m + i0, rem, mo);
+        store8_bf16(d.v + i0, rem, vo);
     }
 }
 
@@ -99,10 +94,13 @@ __global__ void __launch_bounds__(kThreads, 4) step16_kernel(const __grid_consta
 cudaError_t launch_step16(const Step16Args& a, cudaStream_t st)
 {
     static int full = 0;
-    if (full == 0) full = resident_ctas(reinterpret_cast<const void*>(step16_kernel), kThreads, 0);
+    if (full == 0) full = resident_ctas(reinterpret_cast<const void*>(step16_kernel<true>), kThreads, 0);
     if (full <= 0) return cudaErrorUnknown;
     const int grid = a.nblocks < full ? a.nblocks : full;
-    if (grid > 0) step16_kernel<<<grid, kThreads, 0, st>>>(a);
+    if (grid > 0) {
+        if (a.s.sr) step16_kernel<true><<<grid, kThreads, 0, st>>>(a);
+        else step16_kernel<false><<<grid, kThreads, 0, st>>>(a);
+    }
     return cudaGetLastError();
 }
 

@@ -83,8 +83,9 @@ struct HostTables {
         build_codebook(Q8_UNSIGNED, t.cu);
         build_midpoints(t.cs, mid_s);
         build_midpoints(t.cu, mid_u);
+        std::memset(t.cell_s, 0, sizeof(t.cell_s));
         ok = build_cells(mid_s, kSignedL, kCellsSigned, 0, t.cell_s)
-          && build_cells(mid_s, kSignedL, kCellsSigned, 1, t.cell_s + kCellsSigned)
+          && build_cells(mid_s, kSignedL, kCellsSigned, 1, t.cell_s + kSignedHalf)
           && build_cells(mid_u, kUnsignedL, kCellsUnsigned, 0, t.cell_u);
     }
 };

@@ -68,10 +68,11 @@ enum {
  *   rounds every BF16 write stochastically, sr = 0 rounds to nearest even.
  * The step forms, in double, a_t = lr*sqrt(1-beta2^t)/(1-beta1^t),
  * eps_t = eps*sqrt(1-beta2^t) and decay = 1 - lr*weight_decay, rounds each to
- * float once, and per element computes in fp32 (each operation rounded):
- *   m = beta1*m + (1-beta1)*g;  v = beta2*v + (1-beta2)*g*g;
- *   p = p*decay - a_t * m / (sqrt(v) + eps_t)
- * which equals textbook AdamW with decoupled weight decay ([LLM] TL;DR).
+ * float once, and per element computes in fp32, each multiply-add fused
+ * (one rounding) and every other operation rounded on its own:
+ *   m = fma(beta1, m, (1-beta1)*g);  v = fma(beta2, v, (1-beta2)*(g*g));
+ *   p = fma(-a_t, m / (sqrt(v) + eps_t), p*decay)
+ * which is textbook AdamW with decoupled weight decay ([LLM] TL;DR).
  */
 typedef struct {
     double lr, beta1, beta2, eps, weight_decay;

@@ -293,7 +293,12 @@ float q8o_bf16_to_f32(uint16_t h) { return bits_f32((uint32_t)h << 16); }
 /*   a_t = lr*sqrt(1-b2^t)/(1-b1^t),  eps_t = eps*sqrt(1-b2^t)               */
 /* which is exactly lr*mhat/(sqrt(vhat)+eps) with mhat = m/(1-b1^t) and     */
 /* vhat = v/(1-b2^t).  Scalars are formed in double (b^t by libm pow) and   */
-/* rounded once to float; each float operation rounds on its own (no FMA).  */
+/* rounded once to float.  In fp32, each "x*y + z" above is one fused       */
+/* multiply-add (fmaf: one rounding), every other operation rounds on its   */
+/* own:                                                                      */
+/*   m = fma(b1, m, (1-b1)*g)                                                */
+/*   v = fma(b2, v, (1-b2)*(g*g))                                            */
+/*   p = fma(-a_t, m / (sqrt(v) + eps_t), p*decay)                           */
 /* ------------------------------------------------------------------------ */
 
 typedef struct {
@@ -323,20 +328,17 @@ void q8o_step_scalars(const q8o_hparams* hp, q8o_scalars* s)
 /* One element: returns the new fp32 parameter, updates *m and *v in place. */
 float q8o_adamw_element(const q8o_scalars* s, float g, float p, float* m, float* v)
 {
-    float m1 = s->b1 * *m;
-    float m2 = s->omb1 * g;
-    float mn = m1 + m2;
+    float mg = s->omb1 * g;
+    float mn = fmaf(s->b1, *m, mg);
     float gg = g * g;
-    float v1 = s->b2 * *v;
-    float v2 = s->omb2 * gg;
-    float vn = v1 + v2;
+    float vg = s->omb2 * gg;
+    float vn = fmaf(s->b2, *v, vg);
     float den = sqrtf(vn) + s->eps_t;
     float ratio = mn / den;
-    float upd = s->step_size * ratio;
     float pd = p * s->decay;
     *m = mn;
     *v = vn;
-    return pd - upd;
+    return fmaf(-s->step_size, ratio, pd);
 }
 
 static uint16_t round_param(const q8o_hparams* hp, float x, uint32_t stream, uint64_t E)

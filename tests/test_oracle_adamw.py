@@ -8,6 +8,8 @@ is pinned by hand-worked exact cases, by the bias-correction closed form at
 step 1 and by a 60-digit evaluation of the textbook formula
 p*(1 - lr*wd) - lr * mhat / (sqrt(vhat) + eps).
 """
+from fractions import Fraction as Fr
+
 import mpmath
 import numpy as np
 import pytest
@@ -206,3 +208,36 @@ def test_bf16_state_variant():
             lo = int(np.array([want], np.float32).view(np.uint32)[0] >> 16)
             assert got in (lo, lo + 1)
     assert np.all(f(st.v) >= 0)
+
+
+def _round_f32(q):
+    """Nearest float32 to the exact rational q (ties to even)."""
+    x = np.float32(float(q))
+    cands = [np.nextafter(x, np.float32(-np.inf)), x, np.nextafter(x, np.float32(np.inf))]
+    best = min(cands, key=lambda c: (abs(Fr(float(c)) - q), int(np.array([c], np.float32).view(np.uint32)[0]) & 1))
+    return np.float32(best)
+
+
+def test_multiply_adds_are_fused():
+    """Each multiply-add of the update rounds once (fmaf): checked against
+    exact rational arithmetic on inputs where fused and unfused differ."""
+    rng = np.random.default_rng(9)
+    hp = o.hparams(lr=6e-4, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.1, step=3)
+    s = o.step_scalars(hp)
+    fused_differs = 0
+    for _ in range(3000):
+        g = np.float32(rng.standard_normal() * 1e-3)
+        p = np.float32(rng.standard_normal() * 0.02)
+        m = np.float32(rng.standard_normal() * 3e-4)
+        v = np.float32(abs(rng.standard_normal()) * 1e-6)
+        pn, mn, vn = o.adamw_element(s, g, p, m, v)
+        f = lambda z: Fr(float(z))
+        want_m = _round_f32(f(s.b1) * f(m) + f(np.float32(s.omb1) * g))
+        want_v = _round_f32(f(s.b2) * f(v) + f(np.float32(s.omb2) * np.float32(g * g)))
+        assert mn == want_m and vn == want_v
+        ratio = np.float32(mn / np.float32(np.float32(np.sqrt(vn)) + np.float32(s.eps_t)))
+        want_p = _round_f32(-f(s.step_size) * f(ratio) + f(np.float32(p * np.float32(s.decay))))
+        assert pn == want_p
+        unfused = np.float32(np.float32(p * np.float32(s.decay)) - np.float32(np.float32(s.step_size) * ratio))
+        fused_differs += int(unfused != pn)
+    assert fused_differs > 0          # the cases do tell the two readings apart
