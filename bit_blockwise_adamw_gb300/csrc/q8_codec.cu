@@ -52,9 +52,8 @@ __global__ void __launch_bounds__(kThreads) quantize_kernel(const float* __restr
         uint32_t q[2] = {0, 0};
 #pragma unroll
         for (int j = 0; j < kVec; ++j) {
-            const float y = __fmul_rn(xv[j], inv);
-            const uint32_t c = M > 0.0f ? (KIND == Q8_SIGNED ? code_signed(y, s_cell)
-                                                             : code_unsigned(y, s_cell))
+            const uint32_t c = M > 0.0f ? (KIND == Q8_SIGNED ? code_signed_scaled(xv[j], inv, s_cell)
+                                                             : code_unsigned_scaled(xv[j], inv, s_cell))
                                         : kZero;
             q[j >> 2] |= (c & 0xFFu) << ((j & 3) * 8);
         }

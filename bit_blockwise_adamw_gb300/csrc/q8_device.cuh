@@ -73,16 +73,25 @@ __device__ __forceinline__ void draws8(uint64_t E, uint32_t sid, const Scalars& 
 // optimizers", feature request): add a uniform 16-bit draw to the bit pattern
 // and keep the top half; NaN becomes 0x7FC0.  These return the 32-bit pattern
 // whose top half is the bf16 result, so two results pack with one permute.
+//
+// NaN: the fp32 values rounded here are results of GPU arithmetic, whose NaN
+// is the canonical 0x7FFFFFFF (the largest positive pattern), so a signed
+// integer min with 0x7FC00000 maps it to the quiet NaN 0x7FC00000 (whose
+// top half survives the add) and leaves every number and infinity alone.
+__device__ __forceinline__ uint32_t quiet_nan(uint32_t u)
+{
+    return static_cast<uint32_t>(min(static_cast<int>(u), 0x7FC00000));
+}
+
 __device__ __forceinline__ uint32_t sr_hi(float x, uint32_t r16)
 {
-    const uint32_t u = __float_as_uint(x) + r16;
-    return (x != x) ? 0x7FC00000u : u;
+    return quiet_nan(__float_as_uint(x)) + r16;
 }
 
 __device__ __forceinline__ uint32_t rne_hi(float x)
 {
-    const uint32_t u = __float_as_uint(x);
-    return (x != x) ? 0x7FC00000u : u + 0x7FFFu + ((u >> 16) & 1u);
+    const uint32_t u = quiet_nan(__float_as_uint(x));
+    return u + 0x7FFFu + ((u >> 16) & 1u);
 }
 
 // Top halves of a and b -> (b_hi << 16) | a_hi.
@@ -131,35 +140,48 @@ __device__ __forceinline__ float adamw(const Scalars& s, float g, float p, float
 }
 
 // ---------------------------------------------------------------- search
-// Code of a normalised value x: the number of codebook midpoints strictly
-// below clamp(x, -1, 1), read from the cell table (layout in q8_internal.h).
-// The result is correct in its low byte; callers pack codes with byte
-// permutes, which ignore the upper bits.
-__device__ __forceinline__ uint32_t code_signed(float x, const uint32_t* cells)
+// Code of a normalised value: the number of codebook midpoints strictly
+// below clamp(y, -1, 1), y = m * RN(1/absmax), read from the cell table
+// (layout in q8_internal.h).  The callers form |y| clamped to [0, 1] with one
+// saturating multiply (mul.sat: NaN gives 0), so the magnitude needs no
+// further clamp, and take the sign from m.  The result is correct in its low
+// byte; codes are packed with byte permutes, which ignore the upper bits.
+__device__ __forceinline__ uint32_t sat_mul_bits(float x, float s)
 {
-    const uint32_t u = __float_as_uint(x);
-    const uint32_t a = min(u & 0x7FFFFFFFu, 0x3F800000u);            // |x| clamped to 1
+    float r;
+    asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(r) : "f"(x), "f"(s));
+    return __float_as_uint(r);
+}
+
+// a: bits of min(|y|, 1); neg: all ones when y < 0, else zero.
+__device__ __forceinline__ uint32_t code_signed_mag(uint32_t a, uint32_t neg, const uint32_t* cells)
+{
     const int cell = __viaddmax_s32(static_cast<int>(a >> kCellShift), kSignedCellBias, 0);
-    const uint32_t neg = static_cast<uint32_t>(static_cast<int>(u) >> 31);
-    const uint32_t e = cells[static_cast<uint32_t>(cell) | (neg & kSignedHalf)];
-    const uint32_t xs = (a ^ neg) << 16;                              // low 16 bits, complemented if x < 0
+    const uint32_t e = cells[cell + static_cast<int>(neg & static_cast<uint32_t>(kSignedHalf))];
+    const uint32_t xs = (a ^ neg) << 16;                              // low 16 bits, complemented if y < 0
     return e + (xs > e ? 1u : 0u);
 }
 
-// Unsigned book, non-negative x only (the second moment is never negative).
-__device__ __forceinline__ uint32_t code_unsigned_nonneg(float x, const uint32_t* cells)
+// m scaled by inv (= RN(1/absmax) > 0): code in the signed book.
+__device__ __forceinline__ uint32_t code_signed_scaled(float m, float inv, const uint32_t* cells)
 {
-    const uint32_t a = min(__float_as_uint(x), 0x3F800000u);
+    const uint32_t a = sat_mul_bits(fabsf(m), inv);
+    const uint32_t neg = static_cast<uint32_t>(static_cast<int>(__float_as_uint(m)) >> 31);
+    return code_signed_mag(a, neg, cells);
+}
+
+// a: bits of a value in [0, 1] (unsigned book).
+__device__ __forceinline__ uint32_t code_unsigned_mag(uint32_t a, const uint32_t* cells)
+{
     const int cell = __viaddmax_s32(static_cast<int>(a >> kCellShift), kUnsignedCellBias, 0);
     const uint32_t e = cells[cell];
     return e + ((a << 16) > e ? 1u : 0u);
 }
 
-// Unsigned book, any x: negative values (and -0) code as +0.
-__device__ __forceinline__ uint32_t code_unsigned(float x, const uint32_t* cells)
+// v scaled by inv: code in the unsigned book (negative values code as 0).
+__device__ __forceinline__ uint32_t code_unsigned_scaled(float v, float inv, const uint32_t* cells)
 {
-    const int u = max(static_cast<int>(__float_as_uint(x)), 0);
-    return code_unsigned_nonneg(__int_as_float(u), cells);
+    return code_unsigned_mag(sat_mul_bits(v, inv), cells);
 }
 
 // Four codes (low bytes of q0..q3) -> one word, q0 in the lowest byte.

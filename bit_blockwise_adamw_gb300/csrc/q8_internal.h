@@ -28,7 +28,7 @@ constexpr int kSmall = 4096;
 // Entry layout (uint32): bits 0..7 = base code, bits 16..31 = the low 16 bits
 // of the in-cell midpoint's magnitude (complemented for the negative half),
 // 0xFFFF when the cell holds no midpoint.  cell = max((|x| bits >> 16) + bias,
-// 0); the signed table keeps negative x at index cell | kSignedHalf.
+// 0); the signed table keeps negative x at index cell + kSignedHalf.
 constexpr int kCellShift = 16;
 constexpr int kSignedL = 21;      // smallest signed midpoint is 5e-7 > 2^-21
 constexpr int kUnsignedL = 25;    // smallest unsigned midpoint is 5e-8 > 2^-25
@@ -36,8 +36,7 @@ constexpr int kCellsSigned = 2 + kSignedL * 128;     // per sign
 constexpr int kCellsUnsigned = 2 + kUnsignedL * 128; // non-negative half only
 constexpr int kSignedCellBias = 1 - ((127 - kSignedL) << 7);
 constexpr int kUnsignedCellBias = 1 - ((127 - kUnsignedL) << 7);
-constexpr int kSignedHalf = 4096;                    // power of two > kCellsSigned
-static_assert(kSignedHalf >= kCellsSigned && (kSignedHalf & (kSignedHalf - 1)) == 0, "sign bit of the index");
+constexpr int kSignedHalf = kCellsSigned;            // negative half follows the positive one
 constexpr int kCellSEntries = kSignedHalf + kCellsSigned;
 
 struct alignas(16) DevTables {

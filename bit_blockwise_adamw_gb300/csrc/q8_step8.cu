@@ -8,8 +8,8 @@
 // Layout: a persistent grid of resident CTAs (a multiple of the SM count);
 // each CTA stages the codebooks and the cell search tables in shared memory
 // once, then walks a contiguous range of 2048-element blocks.  Per block each
-// of its 256 threads owns eight contiguous elements: 16-byte streaming loads
-// of grad and param, 8-byte loads of each code array.  The kernel is bound by
+// of its 128 threads owns sixteen contiguous elements: 16-byte streaming
+// loads of grad, param and both code arrays.  The kernel is bound by
 // instruction issue rather than by DRAM, so the loop is written to keep the
 // instruction count down: packed fp32x2 arithmetic, one shared-memory lookup
 // per code, warp reductions with redux.sync, uniform branches only.
@@ -29,22 +29,30 @@ __device__ __forceinline__ int find_tensor(const int32_t* start, int nt, int gb)
     return lo;
 }
 
-constexpr int kSmemBytes = static_cast<int>(sizeof(DevTables)) + 2 * kWarps * 8;
+// Each CTA of 128 threads owns one 2048-element block per iteration, sixteen
+// contiguous elements per thread: per-block work (tensor lookup, absmax
+// reduction, reciprocals) is spread over twice as many elements as with
+// eight, and every code load is a full 16-byte vector.
+constexpr int kT8 = 128;
+constexpr int kV8 = 16;
+constexpr int kW8 = kT8 / 32;
+static_assert(kT8 * kV8 == kBlock, "one block per CTA iteration");
+constexpr int kSmemBytes = static_cast<int>(sizeof(DevTables)) + 2 * kW8 * 8;
 
-struct Frag {                  // one thread's eight elements of one block
-    uint32_t g[4], p[4], mc[2], vc[2];
+struct Frag {                  // one thread's sixteen elements of one block
+    uint32_t g[8], p[8], mc[4], vc[4];
 };
 
-// Element-wise loads of a ragged tail (rem < 8 valid elements), zero padded.
+// Element-wise loads of a ragged tail (rem < 16 valid elements), zero padded.
 // Fully unrolled with predicates so the fragment stays in registers.
 __device__ __forceinline__ void load_ragged(const Desc8& d, int64_t i0, int64_t rem, Frag& f)
 {
 #pragma unroll
-    for (int j = 0; j < 4; ++j) { f.g[j] = 0; f.p[j] = 0; }
-    f.mc[0] = f.mc[1] = 0x7F7F7F7Fu;
-    f.vc[0] = f.vc[1] = 0;
+    for (int j = 0; j < 8; ++j) { f.g[j] = 0; f.p[j] = 0; }
 #pragma unroll
-    for (int j = 0; j < kVec; ++j) {
+    for (int j = 0; j < 4; ++j) { f.mc[j] = 0x7F7F7F7Fu; f.vc[j] = 0; }
+#pragma unroll
+    for (int j = 0; j < kV8; ++j) {
         if (j < rem) {
             const uint32_t sh = (j & 1) * 16;
             f.g[j >> 1] |= static_cast<uint32_t>(d.g[i0 + j]) << sh;
@@ -56,21 +64,51 @@ __device__ __forceinline__ void load_ragged(const Desc8& d, int64_t i0, int64_t 
     }
 }
 
-__device__ __forceinline__ void store_ragged(const Desc8& d, int64_t i0, int64_t rem, const uint32_t po[4],
-                                             const uint32_t mo[2], const uint32_t vo[2])
+__device__ __forceinline__ void store_ragged(const Desc8& d, int64_t i0, int64_t rem, const uint32_t po[8],
+                                             const uint32_t mo[4], const uint32_t vo[4])
 {
 #pragma unroll
-    for (int j = 0; j < kVec; ++j) {
+    for (int j = 0; j < kV8; ++j) {
         if (j < rem) {
-            d.p[i0 + j] = static_cast<uint16_t>(po[j >> 1] >> ((j & 1) * 16));
+            d.p[i0 + j] = static_cast<uint16_t>(po[j >> 1] >> ((j & 1) * 16));   // po: written after the barrier
             d.mq[i0 + j] = static_cast<uint8_t>(mo[j >> 2] >> ((j & 3) * 8));
             d.vq[i0 + j] = static_cast<uint8_t>(vo[j >> 2] >> ((j & 3) * 8));
         }
     }
 }
 
+// Ask the L2 to fetch [p, p + bytes) from DRAM now (a hint: it completes
+// asynchronously and is never waited for).  bytes must be a multiple of 16.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Prefetch every input of block `pb` (tensor `tp`) into L2: grad, param and
+// both code arrays, clipped to whole 16-byte chunks inside the tensor.
+__device__ __forceinline__ void prefetch_block(const Desc8& d, int lb)
+{
+    const int64_t first = static_cast<int64_t>(lb) * kBlock;
+    const int64_t n = d.n - first < kBlock ? d.n - first : kBlock;
+    const uint32_t b16 = static_cast<uint32_t>(n * 2) & ~15u;
+    const uint32_t b8 = static_cast<uint32_t>(n) & ~15u;
+    if (b16) {
+        prefetch_l2(d.g + first, b16);
+        prefetch_l2(d.p + first, b16);
+    }
+    if (b8) {
+        prefetch_l2(d.mq + first, b8);
+        prefetch_l2(d.vq + first, b8);
+    }
+}
+
+__device__ __forceinline__ float absmax4(float2 a, float2 b)
+{
+    return fmaxf(max3(fabsf(a.x), fabsf(a.y), fabsf(b.x)), fabsf(b.y));
+}
+
 template <bool SR>
-__global__ void __launch_bounds__(kThreads, 4) step8_kernel(const __grid_constant__ Step8Args a)
+__global__ void __launch_bounds__(kT8, 6) step8_kernel(const __grid_constant__ Step8Args a)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     const DevTables* tabs = reinterpret_cast<const DevTables*>(smem);
@@ -78,12 +116,12 @@ __global__ void __launch_bounds__(kThreads, 4) step8_kernel(const __grid_constan
     const float* s_cu = tabs->cu;
     const uint32_t* s_cell_s = tabs->cell_s;
     const uint32_t* s_cell_u = tabs->cell_u;
-    uint2* s_red = reinterpret_cast<uint2*>(smem + sizeof(DevTables));   // [2][kWarps]
+    uint2* s_red = reinterpret_cast<uint2*>(smem + sizeof(DevTables));   // [2][kW8]
 
     {
         const uint4* src = reinterpret_cast<const uint4*>(a.tab);
         uint4* dst = reinterpret_cast<uint4*>(smem);
-        for (int i = threadIdx.x; i < static_cast<int>(sizeof(DevTables) / 16); i += kThreads) dst[i] = src[i];
+        for (int i = threadIdx.x; i < static_cast<int>(sizeof(DevTables) / 16); i += kT8) dst[i] = src[i];
     }
     __syncthreads();
 
@@ -94,37 +132,59 @@ __global__ void __launch_bounds__(kThreads, 4) step8_kernel(const __grid_constan
     const int begin = static_cast<int>((static_cast<int64_t>(blockIdx.x) * a.nblocks) / gridDim.x);
     const int end = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * a.nblocks) / gridDim.x);
     int ti = begin < end ? find_tensor(a.blk_start, a.nt, begin) : 0;
+    // L2 prefetch cursor: thread 0 keeps kAhead blocks in flight ahead of the
+    // block being computed, so the block's loads find their lines in L2.
+    constexpr int kAhead = 2;
+    int pb = begin, tp = ti;
+    if (tid == 0) {
+        for (; pb < end && pb < begin + kAhead; ++pb) {
+            while (pb >= a.blk_start[tp + 1]) ++tp;
+            prefetch_block(a.d[tp], pb - a.blk_start[tp]);
+        }
+    }
 
     for (int gb = begin, it = 0; gb < end; ++gb, ++it) {
+        if (tid == 0 && pb < end) {
+            while (pb >= a.blk_start[tp + 1]) ++tp;
+            prefetch_block(a.d[tp], pb - a.blk_start[tp]);
+            ++pb;
+        }
         while (gb >= a.blk_start[ti + 1]) ++ti;
         const Desc8& d = a.d[ti];
         const int lb = gb - a.blk_start[ti];
-        const int64_t i0 = static_cast<int64_t>(lb) * kBlock + tid * kVec;
+        const int64_t i0 = static_cast<int64_t>(lb) * kBlock + tid * kV8;
         const int64_t rem = d.n - i0;                    // elements from i0 to the end
-        const bool full = rem >= kVec;
+        const bool full = rem >= kV8;
         const float2 Mold = splat(d.ma[lb]);
         const float2 Vold = splat(d.va[lb]);
 
         Frag f;
         if (full) {
-            const uint4 g4 = ld_stream16(d.g + i0);
-            const uint4 p4 = ld_stream16(d.p + i0);
-            const uint2 m2 = ld_stream8(d.mq + i0);
-            const uint2 v2 = ld_stream8(d.vq + i0);
-            f.g[0] = g4.x; f.g[1] = g4.y; f.g[2] = g4.z; f.g[3] = g4.w;
-            f.p[0] = p4.x; f.p[1] = p4.y; f.p[2] = p4.z; f.p[3] = p4.w;
-            f.mc[0] = m2.x; f.mc[1] = m2.y; f.vc[0] = v2.x; f.vc[1] = v2.y;
+            const uint4 g0 = ld_stream16(d.g + i0), g1 = ld_stream16(d.g + i0 + 8);
+            const uint4 p0 = ld_stream16(d.p + i0), p1 = ld_stream16(d.p + i0 + 8);
+            const uint4 mq = ld_stream16(d.mq + i0);
+            const uint4 vq = ld_stream16(d.vq + i0);
+            f.g[0] = g0.x; f.g[1] = g0.y; f.g[2] = g0.z; f.g[3] = g0.w;
+            f.g[4] = g1.x; f.g[5] = g1.y; f.g[6] = g1.z; f.g[7] = g1.w;
+            f.p[0] = p0.x; f.p[1] = p0.y; f.p[2] = p0.z; f.p[3] = p0.w;
+            f.p[4] = p1.x; f.p[5] = p1.y; f.p[6] = p1.z; f.p[7] = p1.w;
+            f.mc[0] = mq.x; f.mc[1] = mq.y; f.mc[2] = mq.z; f.mc[3] = mq.w;
+            f.vc[0] = vq.x; f.vc[1] = vq.y; f.vc[2] = vq.z; f.vc[3] = vq.w;
         } else {
             load_ragged(d, i0, rem > 0 ? rem : 0, f);
         }
 
         // dequantize and update, two elements at a time
-        float2 m[4], v[4];
-        uint32_t po[4];
-        uint32_t r[4] = {0, 0, 0, 0};
-        if constexpr (SR) draws8(d.e0 + static_cast<uint64_t>(i0), 0u, s, r);
+        float2 m[8], v[8];
+        uint32_t po[8];
+        uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+        if constexpr (SR) {
+            const uint64_t E = d.e0 + static_cast<uint64_t>(i0);
+            draws8(E, 0u, s, r);
+            draws8(E + 8, 0u, s, r + 4);
+        }
 #pragma unroll
-        for (int k = 0; k < 4; ++k) {
+        for (int k = 0; k < 8; ++k) {
             const uint32_t cw = f.mc[k >> 1], vw = f.vc[k >> 1];
             const int b0 = (k & 1) * 2;
             m[k] = __fmul2_rn(make_float2(s_cs[byte_of(cw, b0)], s_cs[byte_of(cw, b0 + 1)]), Mold);
@@ -133,62 +193,62 @@ __global__ void __launch_bounds__(kThreads, 4) step8_kernel(const __grid_constan
             po[k] = round2<SR>(pn, r[k]);
         }
 
+        // the parameters do not wait for the block absmax: store them now
+        if (full) {
+            st_stream16(d.p + i0, make_uint4(po[0], po[1], po[2], po[3]));
+            st_stream16(d.p + i0 + 8, make_uint4(po[4], po[5], po[6], po[7]));
+        }
+
         // block absmax of the new moments (padding elements do not count)
         if (!full) {
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
+            for (int k = 0; k < 8; ++k) {
                 if (2 * k >= rem) { m[k].x = 0.0f; v[k].x = 0.0f; }
                 if (2 * k + 1 >= rem) { m[k].y = 0.0f; v[k].y = 0.0f; }
             }
         }
-        const float lm = fmaxf(max3(fabsf(m[0].x), fabsf(m[0].y), fabsf(m[1].x)),
-                               max3(fabsf(m[1].y), fabsf(m[2].x), max3(fabsf(m[2].y), fabsf(m[3].x), fabsf(m[3].y))));
-        const float lv = fmaxf(max3(v[0].x, v[0].y, v[1].x), max3(v[1].y, v[2].x, max3(v[2].y, v[3].x, v[3].y)));
+        const float lm = fmaxf(fmaxf(absmax4(m[0], m[1]), absmax4(m[2], m[3])),
+                               fmaxf(absmax4(m[4], m[5]), absmax4(m[6], m[7])));
+        const float lv = fmaxf(fmaxf(absmax4(v[0], v[1]), absmax4(v[2], v[3])),
+                               fmaxf(absmax4(v[4], v[5]), absmax4(v[6], v[7])));
         // non-negative floats order like their bit patterns
         const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(lm));
         const uint32_t wv = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(lv));
-        uint2* red = s_red + (it & 1) * kWarps;          // double-buffered: one barrier per block
+        uint2* red = s_red + (it & 1) * kW8;             // double-buffered: one barrier per block
         if (lane == 0) red[warp] = make_uint2(wm, wv);
         __syncthreads();
-        const uint2 t = lane < kWarps ? red[lane] : make_uint2(0u, 0u);
+        const uint2 t = lane < kW8 ? red[lane] : make_uint2(0u, 0u);
         const float M = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, t.x));
         const float V = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, t.y));
 
         // requantize against the new absmax: scale by RN(1/absmax), look up
-        uint32_t mo[2], vo[2];
+        uint32_t mo[4], vo[4];
         if (M > 0.0f) {
-            const float2 im = splat(__frcp_rn(M));
-            uint32_t q[8];
+            const float im = __frcp_rn(M);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 x = __fmul2_rn(m[k], im);
-                q[2 * k] = code_signed(x.x, s_cell_s);
-                q[2 * k + 1] = code_signed(x.y, s_cell_s);
+            for (int k = 0; k < 8; k += 2) {
+                mo[k >> 1] = pack4(code_signed_scaled(m[k].x, im, s_cell_s), code_signed_scaled(m[k].y, im, s_cell_s),
+                                   code_signed_scaled(m[k + 1].x, im, s_cell_s),
+                                   code_signed_scaled(m[k + 1].y, im, s_cell_s));
             }
-            mo[0] = pack4(q[0], q[1], q[2], q[3]);
-            mo[1] = pack4(q[4], q[5], q[6], q[7]);
         } else {
-            mo[0] = mo[1] = 0x7F7F7F7Fu;
+            mo[0] = mo[1] = mo[2] = mo[3] = 0x7F7F7F7Fu;
         }
         if (V > 0.0f) {
-            const float2 iv = splat(__frcp_rn(V));
-            uint32_t q[8];
+            const float iv = __frcp_rn(V);
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const float2 x = __fmul2_rn(v[k], iv);
-                q[2 * k] = code_unsigned_nonneg(x.x, s_cell_u);
-                q[2 * k + 1] = code_unsigned_nonneg(x.y, s_cell_u);
+            for (int k = 0; k < 8; k += 2) {
+                vo[k >> 1] = pack4(code_unsigned_scaled(v[k].x, iv, s_cell_u), code_unsigned_scaled(v[k].y, iv, s_cell_u),
+                                   code_unsigned_scaled(v[k + 1].x, iv, s_cell_u),
+                                   code_unsigned_scaled(v[k + 1].y, iv, s_cell_u));
             }
-            vo[0] = pack4(q[0], q[1], q[2], q[3]);
-            vo[1] = pack4(q[4], q[5], q[6], q[7]);
         } else {
-            vo[0] = vo[1] = 0u;
+            vo[0] = vo[1] = vo[2] = vo[3] = 0u;
         }
 
         if (full) {
-            st_stream16(d.p + i0, make_uint4(po[0], po[1], po[2], po[3]));
-            st_stream8(d.mq + i0, make_uint2(mo[0], mo[1]));
-            st_stream8(d.vq + i0, make_uint2(vo[0], vo[1]));
+            st_stream16(d.mq + i0, make_uint4(mo[0], mo[1], mo[2], mo[3]));
+            st_stream16(d.vq + i0, make_uint4(vo[0], vo[1], vo[2], vo[3]));
         } else if (rem > 0) {
             store_ragged(d, i0, rem, po, mo, vo);
         }
@@ -242,11 +302,11 @@ cudaError_t launch_step8_t(const Step8Args& a, cudaStream_t st)
         const void* k = reinterpret_cast<const void*>(step8_kernel<SR>);
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
-        full = resident_ctas(k, kThreads, kSmemBytes);
+        full = resident_ctas(k, kT8, kSmemBytes);
         if (full <= 0) return cudaErrorUnknown;
     }
     const int grid = a.nblocks < full ? a.nblocks : full;
-    if (grid > 0) step8_kernel<SR><<<grid, kThreads, kSmemBytes, st>>>(a);
+    if (grid > 0) step8_kernel<SR><<<grid, kT8, kSmemBytes, st>>>(a);
     return cudaGetLastError();
 }
 
