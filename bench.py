@@ -42,6 +42,8 @@ def parse():
     ap.add_argument("--workload", default="gptneo-6.7b")
     ap.add_argument("--flat", type=int, default=0,
                     help="replace the workload by one flat tensor of this many params (profiling)")
+    ap.add_argument("--flat-state", default="8bit", choices=["8bit", "bf16"],
+                    help="optimizer state of the --flat tensor")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
@@ -63,9 +65,9 @@ def load_peaks():
 def workload(args):
     from bit_blockwise_adamw_gb300 import workloads as W
     if args.flat:
-        return W.custom("flat-%d" % args.flat, [args.flat], steps=args.steps, grad_std=1e-4,
-                        outlier_rate=1e-4, outlier_factor=1000.0,
-                        hp=dict(lr=6e-4, weight_decay=0.1), data_seed=1003)
+        return W.custom("flat-%d-%s" % (args.flat, args.flat_state), [args.flat], steps=args.steps,
+                        grad_std=1e-4, outlier_rate=1e-4, outlier_factor=1000.0,
+                        hp=dict(lr=6e-4, weight_decay=0.1), data_seed=1003, state=args.flat_state)
     return W.WORKLOADS[args.workload]
 
 
