@@ -189,6 +189,17 @@ class Tensor8:
         return cls(param, grad, m32=torch.zeros(n, dtype=torch.float32, device=dev),
                    v32=torch.zeros(n, dtype=torch.float32, device=dev), philox_offset=philox_offset)
 
+    def slice(self, start: int, count: int, philox_offset: int):
+        """Block-aligned slice [start, start + count) of this tensor with the
+        given global Philox offset (the 8-bit state stays on the 8-bit path)."""
+        assert self.m_codes is not None, "slices are taken of 8-bit state"
+        assert start % BLOCK == 0 and 0 <= start and start + count <= self.param.numel()
+        b0, b1 = start // BLOCK, (start + count + BLOCK - 1) // BLOCK
+        sl = slice(start, start + count)
+        return Tensor8(self.param[sl], None if self.grad is None else self.grad[sl],
+                       self.m_codes[sl], self.v_codes[sl], self.m_absmax[b0:b1], self.v_absmax[b0:b1],
+                       philox_offset=philox_offset)
+
     def _struct(self):
         assert self.param.dtype == torch.bfloat16 and self.grad.dtype == torch.bfloat16
         assert self.grad.numel() == self.param.numel()

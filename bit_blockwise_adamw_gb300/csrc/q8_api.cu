@@ -78,7 +78,7 @@ int check_offset(int64_t e0, int64_t numel, int i)
 
 extern "C" {
 
-int q8_abi_version(void) { return 1; }
+int q8_abi_version(void) { return 2; }
 
 const char* q8_last_error(void) { return g_error.c_str(); }
 
@@ -166,14 +166,16 @@ int adamw8bit_sr_step(const q8_tensor8* list, int ntensors, const q8_adamw_hpara
         if (!t.param || !t.grad) return fail(Q8_ERR_NULL, at("param and grad must be non-NULL", i));
         if (!aligned(t.param, 16) || !aligned(t.grad, 16))
             return fail(Q8_ERR_ALIGN, at("param and grad must be 16-byte aligned", i));
-        if (t.numel >= q8::kSmall) {
-            if (!t.m_codes || !t.v_codes || !t.m_absmax || !t.v_absmax)
+        if (t.m_codes) {
+            if (t.m32 || t.v32) return fail(Q8_ERR_ARG, at("an entry carries either 8-bit or fp32 state", i));
+            if (!t.v_codes || !t.m_absmax || !t.v_absmax)
                 return fail(Q8_ERR_NULL, at("8-bit state pointers must be non-NULL", i));
             if (!aligned(t.m_codes, 16) || !aligned(t.v_codes, 16) || !aligned(t.m_absmax, 4) ||
                 !aligned(t.v_absmax, 4))
                 return fail(Q8_ERR_ALIGN, at("codes must be 16-byte and absmax 4-byte aligned", i));
         } else {
-            if (!t.m32 || !t.v32) return fail(Q8_ERR_NULL, at("m32 and v32 must be non-NULL", i));
+            if (!t.m32 || !t.v32) return fail(Q8_ERR_NULL, at("state pointers (codes or m32/v32) are NULL", i));
+            if (t.numel >= q8::kSmall) return fail(Q8_ERR_SIZE, at("fp32 state needs numel < 4096", i));
             if (!aligned(t.m32, 16) || !aligned(t.v32, 16))
                 return fail(Q8_ERR_ALIGN, at("m32 and v32 must be 16-byte aligned", i));
         }
@@ -213,7 +215,7 @@ int adamw8bit_sr_step(const q8_tensor8* list, int ntensors, const q8_adamw_hpara
         const uint64_t e0 = static_cast<uint64_t>(t.philox_offset >= 0 ? t.philox_offset : running);
         running += t.numel;
         if (t.numel == 0) continue;
-        if (t.numel >= q8::kSmall) {
+        if (t.m_codes) {
             const int64_t nb = (t.numel + q8::kBlock - 1) / q8::kBlock;
             if (big->nt == q8::kMaxList ||
                 static_cast<int64_t>(big->blk_start[big->nt]) + nb > std::numeric_limits<int32_t>::max()) {

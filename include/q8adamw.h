@@ -56,7 +56,7 @@ typedef enum { Q8_SIGNED = 0, Q8_UNSIGNED = 1 } q8_kind;
 
 enum {
     Q8_BLOCK = 2048,          /* [BW] method bullets: elements per absmax block */
-    Q8_SMALL_NUMEL = 4096,    /* tensors below this keep fp32 state ([SR])      */
+    Q8_SMALL_NUMEL = 4096,    /* tensors below this are given fp32 state ([SR]) */
     Q8_MAX_STEP = 0x7FFFFFFF  /* the step counter enters Philox as 32 bits      */
 };
 
@@ -89,14 +89,19 @@ typedef struct {
  *   philox_offset  global Philox index of element 0; a negative value means
  *                  "the sum of numel over the tensors before this one in the
  *                  list" (so one list behaves like one flat tensor)
- * numel >= 4096 (8-bit state, [BW]): m_codes, v_codes are uint8 indices into
+ * The state an entry carries picks its path:
+ * 8-bit state ([BW]; m_codes != NULL): m_codes, v_codes are uint8 indices into
  *   the signed / unsigned codebooks; m_absmax, v_absmax hold one float per
  *   2048-element block (ceil(numel/2048) entries, 4-byte aligned).  m32/v32
- *   are ignored.  An all-zero state (codes anything, absmax 0) is the fresh
- *   state; canonical zero codes are 127 (m) and 0 (v).
- * numel < 4096 (fp32 state, [SR] scoping comment): m32, v32 are float arrays
- *   of numel elements, updated in place; the 8-bit fields are ignored.
- * numel == 0 tensors are skipped.
+ *   must be NULL.  An all-zero state (codes anything, absmax 0) is the fresh
+ *   state; canonical zero codes are 127 (m) and 0 (v).  Tensors of 4096 or
+ *   more elements are created with this state; a block-aligned slice of one
+ *   (element offset a multiple of 2048, its absmax pointers advanced to match,
+ *   philox_offset set to the global index of its first element) may be
+ *   shorter and stays on this path.
+ * fp32 state ([SR] scoping comment: small tensors; m_codes == NULL): m32, v32
+ *   are float arrays of numel elements, updated in place; numel < 4096.
+ * numel == 0 entries are skipped.
  */
 typedef struct {
     uint16_t* param;
@@ -157,9 +162,9 @@ int q8_blockwise_dequantize(const uint8_t* codes, const float* absmax, float* x,
  * `ntensors` tensors (host array).  Per 2048-element block: dequantize m, v,
  * run the AdamW update above in fp32, take the new block absmax of m and v,
  * requantize them, and write p rounded to bf16 with the 16-bit Philox draw of
- * element E = philox_offset + i on stream 0 (see q8_philox_fill).  Tensors
- * below 4096 elements take the fp32-state path with the same maths.  Blocks
- * never straddle tensors.  0 <= ntensors; the list may mix both paths.
+ * element E = philox_offset + i on stream 0 (see q8_philox_fill).  Entries
+ * with fp32 state take the fp32-state path with the same maths.  Blocks
+ * never straddle entries.  0 <= ntensors; the list may mix both paths.
  */
 int adamw8bit_sr_step(const q8_tensor8* list, int ntensors, const q8_adamw_hparams* hp,
                       q8_stream_t stream);
@@ -195,7 +200,7 @@ int q8_prepare_device(void);
 const char* q8_last_error(void);
 
 /* ABI version: bumped on any change of a signature or struct. */
-int q8_abi_version(void);
+int q8_abi_version(void);   /* 2 */
 
 #ifdef __cplusplus
 }

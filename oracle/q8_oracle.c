@@ -442,16 +442,19 @@ void q8o_adamw_bf16_tensor(const q8o_tensor16* t, uint64_t E0, const q8o_hparams
     }
 }
 
-/* Whole list.  Tensors below 4096 elements take the fp32-state path, the
- * rest the 8-bit path; a negative philox_offset means the running sum of
- * the numels of the tensors before it in list order. */
+/* Whole list.  [SR] scoping comment: small tensors keep fp32 state.  The
+ * 4096-element threshold decides which state a tensor is created with; in a
+ * step, each entry takes the path of the state it carries (8-bit when it has
+ * codes, fp32 otherwise), so a block-aligned slice of a large tensor stays on
+ * the 8-bit path.  A negative philox_offset means the running sum of the
+ * numels of the entries before it in list order. */
 int q8o_adamw8bit_sr_step(const q8o_tensor8* list, int n, const q8o_hparams* hp)
 {
     uint64_t running = 0;
     for (int i = 0; i < n; ++i) {
         const q8o_tensor8* t = &list[i];
         uint64_t E0 = t->philox_offset >= 0 ? (uint64_t)t->philox_offset : running;
-        if (t->numel >= Q8O_SMALL) q8o_adamw8bit_tensor(t, E0, hp);
+        if (t->m_codes) q8o_adamw8bit_tensor(t, E0, hp);
         else q8o_adamw32_tensor(t, E0, hp);
         running += (uint64_t)t->numel;
     }

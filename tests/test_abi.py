@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version(lib):
-    assert q8.q8_abi_version() == 1
+    assert q8.q8_abi_version() == 2
 
 
 @pytest.mark.parametrize("kind", [q8.SIGNED, q8.UNSIGNED])
@@ -71,9 +71,12 @@ def test_step8_rejects_bad_tensor(lib, field, value, code):
     assert "tensor 1" in q8.q8_last_error()
 
 
-def test_small_tensor_needs_fp32_state(lib):
-    assert _call8(lib, [_t8(numel=100)]) == -1
-    assert _call8(lib, [_t8(numel=100, m32=0x7000, v32=0x7004)]) == -3
+def test_state_picks_the_path(lib):
+    no8 = dict(m_codes=None, v_codes=None, m_absmax=None, v_absmax=None)
+    assert _call8(lib, [_t8(numel=100, **no8)]) == -1                       # no state at all
+    assert _call8(lib, [_t8(numel=100, m32=0x7000, v32=0x7004, **no8)]) == -3
+    assert _call8(lib, [_t8(numel=5000, m32=0x7000, v32=0x7010, **no8)]) == -2   # fp32 state is for < 4096
+    assert _call8(lib, [_t8(numel=100, m32=0x7000, v32=0x7010)]) == -4      # both kinds of state
 
 
 @pytest.mark.parametrize("field,value", [
