@@ -117,15 +117,25 @@ __device__ __forceinline__ uint32_t round2(float2 x, uint32_t r)
 // and the division stay scalar.
 __device__ __forceinline__ float2 splat(float x) { return make_float2(x, x); }
 
+// The moment updates of a pair: m = fma(b1, m, (1-b1)*g), v = fma(b2, v, (1-b2)*g*g).
+__device__ __forceinline__ void moments2(const Scalars& s, float2 g, float2& m, float2& v)
+{
+    m = __ffma2_rn(splat(s.b1), m, __fmul2_rn(splat(s.omb1), g));
+    v = __ffma2_rn(splat(s.b2), v, __fmul2_rn(splat(s.omb2), __fmul2_rn(g, g)));
+}
+
+// The parameter update of a pair given sqrt(v): p*decay - a_t*(m/(sqrt(v)+eps_t)).
+__device__ __forceinline__ float2 param2(const Scalars& s, float2 p, float2 m, float2 root)
+{
+    const float2 ratio = make_float2(__fdiv_rn(m.x, __fadd_rn(root.x, s.eps_t)),
+                                     __fdiv_rn(m.y, __fadd_rn(root.y, s.eps_t)));
+    return __ffma2_rn(splat(-s.step_size), ratio, __fmul2_rn(p, splat(s.decay)));
+}
+
 __device__ __forceinline__ float2 adamw2(const Scalars& s, float2 g, float2 p, float2& m, float2& v)
 {
-    const float2 mn = __ffma2_rn(splat(s.b1), m, __fmul2_rn(splat(s.omb1), g));
-    const float2 vn = __ffma2_rn(splat(s.b2), v, __fmul2_rn(splat(s.omb2), __fmul2_rn(g, g)));
-    const float2 ratio = make_float2(__fdiv_rn(mn.x, __fadd_rn(__fsqrt_rn(vn.x), s.eps_t)),
-                                     __fdiv_rn(mn.y, __fadd_rn(__fsqrt_rn(vn.y), s.eps_t)));
-    m = mn;
-    v = vn;
-    return __ffma2_rn(splat(-s.step_size), ratio, __fmul2_rn(p, splat(s.decay)));
+    moments2(s, g, m, v);
+    return param2(s, p, m, make_float2(__fsqrt_rn(v.x), __fsqrt_rn(v.y)));
 }
 
 // Scalar form (same rounding), for the small-tensor kernel.
@@ -153,13 +163,20 @@ __device__ __forceinline__ uint32_t sat_mul_bits(float x, float s)
     return __float_as_uint(r);
 }
 
-// a: bits of min(|y|, 1); neg: all ones when y < 0, else zero.
+// a: bits of min(|y|, 1); neg: all ones when y < 0, else zero.  The table
+// counts, per magnitude cell, the positive midpoints (indices 127..253) below
+// the cell and holds the low bits of the one inside it.  By the odd symmetry
+// of the signed book, y > 0 takes code 127 + #{positive midpoints < |y|} and
+// y < 0 takes 127 - #{positive midpoints <= |y|}; the comparison key carries
+// 0xFF00 in its low half for y < 0 (above any base count, below the marker of
+// a cell without a midpoint), which turns "<" into "<=".
 __device__ __forceinline__ uint32_t code_signed_mag(uint32_t a, uint32_t neg, const uint32_t* cells)
 {
     const int cell = __viaddmax_s32(static_cast<int>(a >> kCellShift), kSignedCellBias, 0);
-    const uint32_t e = cells[cell + static_cast<int>(neg & static_cast<uint32_t>(kSignedHalf))];
-    const uint32_t xs = (a ^ neg) << 16;                              // low 16 bits, complemented if y < 0
-    return e + (xs > e ? 1u : 0u);
+    const uint32_t e = cells[cell];
+    const uint32_t key = (a << 16) | (neg & 0xFF00u);
+    const uint32_t c = e + (key > e ? 1u : 0u);
+    return 127u + ((c ^ neg) - neg);
 }
 
 // m scaled by inv (= RN(1/absmax) > 0): code in the signed book.
@@ -200,6 +217,7 @@ __device__ __forceinline__ float max3(float a, float b, float c)
     asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
     return r;
 }
+
 
 // Streaming loads/stores: every byte of the step is touched once.
 __device__ __forceinline__ uint4 ld_stream16(const void* p)

@@ -20,29 +20,30 @@ static_assert(kThreads * kVec == kBlock, "one block per CTA iteration");
 constexpr int kWarps = kThreads / 32;
 constexpr int kSmall = 4096;
 
-// Search cells.  |x| <= 1 is split into cells by its binade and the top seven
-// mantissa bits (every 2^16 consecutive bit patterns share a cell); magnitudes
-// below 2^-L form cell 0.  L is chosen so that no midpoint lies in cell 0 and
-// the seven mantissa bits keep at most one midpoint in any cell, so the code
-// is   base(cell) + (x beyond the cell's midpoint).
-// Entry layout (uint32): bits 0..7 = base code, bits 16..31 = the low 16 bits
-// of the in-cell midpoint's magnitude (complemented for the negative half),
-// 0xFFFF when the cell holds no midpoint.  cell = max((|x| bits >> 16) + bias,
-// 0); the signed table keeps negative x at index cell + kSignedHalf.
+// Search cells.  A magnitude |y| <= 1 falls in a cell given by its binade and
+// the top seven mantissa bits (every 2^16 consecutive bit patterns share a
+// cell); magnitudes below 2^-L form cell 0.  L is chosen so that no midpoint
+// lies in cell 0 and the seven mantissa bits keep at most one midpoint in any
+// cell, so the count of midpoints below |y| is
+//   base(cell) + (|y| beyond the cell's midpoint).
+// Entry layout (uint32): bits 0..7 = base count, bits 16..31 = the low 16 bits
+// of the in-cell midpoint; a cell that holds none stores 0xFFFFFF00 | base.  The signed table
+// counts only the positive midpoints (the book is odd-symmetric, so the sign
+// is applied after the lookup); the unsigned table counts all of them.
+// cell = max((|y| bits >> 16) + bias, 0).
 constexpr int kCellShift = 16;
 constexpr int kSignedL = 21;      // smallest signed midpoint is 5e-7 > 2^-21
 constexpr int kUnsignedL = 25;    // smallest unsigned midpoint is 5e-8 > 2^-25
-constexpr int kCellsSigned = 2 + kSignedL * 128;     // per sign
-constexpr int kCellsUnsigned = 2 + kUnsignedL * 128; // non-negative half only
+constexpr int kCellsSigned = 2 + kSignedL * 128;
+constexpr int kCellsUnsigned = 2 + kUnsignedL * 128;
 constexpr int kSignedCellBias = 1 - ((127 - kSignedL) << 7);
 constexpr int kUnsignedCellBias = 1 - ((127 - kUnsignedL) << 7);
-constexpr int kSignedHalf = kCellsSigned;            // negative half follows the positive one
-constexpr int kCellSEntries = kSignedHalf + kCellsSigned;
+constexpr int kCellSEntries = kCellsSigned + 2;      // padded to a multiple of 4 entries
 
 struct alignas(16) DevTables {
     float cs[256];                         // signed codebook (dequantize m)
     float cu[256];                         // unsigned codebook (dequantize v)
-    uint32_t cell_s[kCellSEntries];        // [0, kCellsSigned): x >= 0; [kSignedHalf, ...): x < 0
+    uint32_t cell_s[kCellSEntries];        // positive midpoints 127..253, by |y|
     uint32_t cell_u[kCellsUnsigned];       // non-negative x only
 };
 static_assert(sizeof(DevTables) % 16 == 0, "tables are copied to shared memory 16 bytes at a time");

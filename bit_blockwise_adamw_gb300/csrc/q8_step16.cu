@@ -74,14 +74,20 @@ __global__ void __launch_bounds__(kThreads, 4) step16_kernel(const __grid_consta
             draws8(E, 2u, s, rv);
         }
         uint32_t po[4], mo[4], vo[4];
+        float2 m[4], v[4];
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            float2 m = bf16x2(mw[k]);
-            float2 v = bf16x2(vw[k]);
-            const float2 pn = adamw2(s, bf16x2(gw[k]), bf16x2(pw[k]), m, v);
+            m[k] = bf16x2(mw[k]);
+            v[k] = bf16x2(vw[k]);
+            moments2(s, bf16x2(gw[k]), m[k], v[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const float2 root = make_float2(__fsqrt_rn(v[k].x), __fsqrt_rn(v[k].y));
+            const float2 pn = param2(s, bf16x2(pw[k]), m[k], root);
             po[k] = round2<SR>(pn, rp[k]);
-            mo[k] = round2<SR>(m, rm[k]);
-            vo[k] = round2<SR>(v, rv[k]);
+            mo[k] = round2<SR>(m[k], rm[k]);
+            vo[k] = round2<SR>(v[k], rv[k]);
         }
         store8_bf16(d.p + i0, rem, po);
         store8_bf16(d.m + i0, rem, mo);

@@ -108,7 +108,7 @@ __device__ __forceinline__ float absmax4(float2 a, float2 b)
 }
 
 template <bool SR>
-__global__ void __launch_bounds__(kT8, 6) step8_kernel(const __grid_constant__ Step8Args a)
+__global__ void __launch_bounds__(kT8, 7) step8_kernel(const __grid_constant__ Step8Args a)
 {
     extern __shared__ __align__(16) unsigned char smem[];
     const DevTables* tabs = reinterpret_cast<const DevTables*>(smem);
@@ -189,8 +189,12 @@ __global__ void __launch_bounds__(kT8, 6) step8_kernel(const __grid_constant__ S
             const int b0 = (k & 1) * 2;
             m[k] = __fmul2_rn(make_float2(s_cs[byte_of(cw, b0)], s_cs[byte_of(cw, b0 + 1)]), Mold);
             v[k] = __fmul2_rn(make_float2(s_cu[byte_of(vw, b0)], s_cu[byte_of(vw, b0 + 1)]), Vold);
-            const float2 pn = adamw2(s, bf16x2(f.g[k]), bf16x2(f.p[k]), m[k], v[k]);
-            po[k] = round2<SR>(pn, r[k]);
+            moments2(s, bf16x2(f.g[k]), m[k], v[k]);
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float2 root = make_float2(__fsqrt_rn(v[k].x), __fsqrt_rn(v[k].y));
+            po[k] = round2<SR>(param2(s, bf16x2(f.p[k]), m[k], root), r[k]);
         }
 
         // the parameters do not wait for the block absmax: store them now

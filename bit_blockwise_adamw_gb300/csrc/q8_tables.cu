@@ -42,9 +42,10 @@ void build_midpoints(const float c[256], float mid[255])
 float bits_to_float(uint32_t u) { float f; std::memcpy(&f, &u, 4); return f; }
 uint32_t float_to_bits(float f) { uint32_t u; std::memcpy(&u, &f, 4); return u; }
 
-// Fill one half (sign s) of a cell table; returns false if a cell would hold
-// more than one midpoint (the table could not then decide with one compare).
-bool build_cells(const float mid[255], int L, int ncells, int sign, uint32_t* out)
+// Fill a cell table over magnitudes from the ascending midpoints mid[0..nmid)
+// (all positive); returns false if a cell would hold more than one midpoint
+// (the table could not then decide with one compare).
+bool build_cells(const float* mid, int nmid, int L, int ncells, uint32_t* out)
 {
     const uint32_t low = static_cast<uint32_t>(127 - L) << 23;
     for (int c = 0; c < ncells; ++c) {
@@ -56,19 +57,20 @@ bool build_cells(const float mid[255], int L, int ncells, int sign, uint32_t* ou
         }
         if (a_hi > 0x3F800000u) a_hi = 0x3F800000u;
         if (a_lo > a_hi) a_lo = a_hi;
-        const float x_first = sign ? -bits_to_float(a_hi) : bits_to_float(a_lo);
-        const float x_last = sign ? -bits_to_float(a_lo) : bits_to_float(a_hi);
+        const float x_first = bits_to_float(a_lo);
+        const float x_last = bits_to_float(a_hi);
         uint32_t base = 0;
-        while (base < 255 && mid[base] < x_first) ++base;
+        while (static_cast<int>(base) < nmid && mid[base] < x_first) ++base;
         int inside = 0;
         uint32_t ml = 0xFFFFu;
-        for (int j = static_cast<int>(base); j < 255 && mid[j] <= x_last; ++j) {
+        for (int j = static_cast<int>(base); j < nmid && mid[j] <= x_last; ++j) {
             ++inside;
-            const uint32_t low16 = float_to_bits(std::fabs(mid[j])) & 0xFFFFu;
-            ml = sign ? (~low16 & 0xFFFFu) : low16;
+            ml = float_to_bits(mid[j]) & 0xFFFFu;
         }
         if (inside > 1 || (c == 0 && inside > 0)) return false;
-        out[c] = (ml << 16) | base;
+        // a cell without a midpoint also sets bits 8..15, so that no key (at
+        // most 0xFFFFFF00) ever compares above it
+        out[c] = (ml << 16) | base | (inside ? 0u : 0xFF00u);
     }
     return true;
 }
@@ -84,9 +86,13 @@ struct HostTables {
         build_midpoints(t.cs, mid_s);
         build_midpoints(t.cu, mid_u);
         std::memset(t.cell_s, 0, sizeof(t.cell_s));
-        ok = build_cells(mid_s, kSignedL, kCellsSigned, 0, t.cell_s)
-          && build_cells(mid_s, kSignedL, kCellsSigned, 1, t.cell_s + kSignedHalf)
-          && build_cells(mid_u, kUnsignedL, kCellsUnsigned, 0, t.cell_u);
+        // signed book: positive midpoints mid[127..253] (mid[254] is the pad's
+        // 1.0, never below any |y| <= 1); the book must be odd-symmetric
+        bool symmetric = true;
+        for (int i = 0; i < 127; ++i) symmetric = symmetric && mid_s[126 - i] == -mid_s[127 + i];
+        ok = symmetric
+          && build_cells(mid_s + 127, 127, kSignedL, kCellsSigned, t.cell_s)
+          && build_cells(mid_u, 255, kUnsignedL, kCellsUnsigned, t.cell_u);
     }
 };
 

@@ -39,16 +39,24 @@ def _sweep(kind, stride):
     v = np.concatenate(vals).astype(np.float32)
     per = 2047
     nb = (v.size + per - 1) // per
-    x = np.zeros(nb * 2048, np.float32)
-    x.reshape(nb, 2048)[:, 0] = 1.0
-    body = x.reshape(nb, 2048)[:, 1:].reshape(-1)
+    body = np.zeros(nb * per, np.float32)
     body[:v.size] = v
-    return x
+    x = np.empty((nb, 2048), np.float32)
+    x[:, 0] = 1.0
+    x[:, 1:] = body.reshape(nb, per)
+    assert np.array_equal(x[:, 1:].reshape(-1)[:v.size], v)
+    return x.reshape(-1)
 
 
 @pytest.mark.parametrize("kind", KINDS)
-def test_quantize_dense_sweep(cuda_device, kind):
+@pytest.mark.parametrize("lead", [1.0, 0.75])
+def test_quantize_dense_sweep(cuda_device, kind, lead):
+    """Every 13th float of [0, 1] (both signs for the signed book) and every
+    float near a threshold, quantized in blocks whose first element is `lead`
+    (with 1.0 every block's absmax is 1 and the normalised value is the float
+    itself; with 0.75 most blocks normalise by another absmax)."""
     x = _sweep(kind, 13)
+    x[::2048] = lead
     xd = torch.from_numpy(x).to(cuda_device)
     codes = torch.empty(x.size, dtype=torch.uint8, device=cuda_device)
     absmax = torch.empty(x.size // 2048, dtype=torch.float32, device=cuda_device)
