@@ -87,10 +87,17 @@ def algorithmic_bytes(wl):
 
 
 def launches_per_step(wl):
-    n_big = sum(1 for t in wl.tensors if t.numel >= 4096 or wl.state == "bf16")
-    n_small = sum(1 for t in wl.tensors if t.numel < 4096 and wl.state != "bf16")
+    """Kernel launches of one step: one per chunk of up to 448 tensors, plus,
+    on the 8-bit path, one tail launch for a chunk holding a tensor whose
+    length is not a multiple of 2048."""
     per = 448
-    return (n_big + per - 1) // per + (n_small + per - 1) // per
+    if wl.state == "bf16":
+        return (len(wl.tensors) + per - 1) // per
+    big = [t.numel for t in wl.tensors if t.numel >= 4096]
+    n_small = sum(1 for t in wl.tensors if 0 < t.numel < 4096)
+    chunks = [big[i:i + per] for i in range(0, len(big), per)]
+    tails = sum(1 for c in chunks if any(n % BLOCK for n in c))
+    return len(chunks) + tails + (n_small + per - 1) // per
 
 
 class ClockSampler:

@@ -7,7 +7,9 @@
 //
 // Layout: a persistent grid of resident CTAs (a multiple of the SM count);
 // each CTA stages the codebooks and the cell search tables in shared memory
-// once, then walks a contiguous range of 2048-element blocks.  Per block each
+// once, then walks a contiguous range of 2048-element blocks.  The partial
+// last block of a tensor (if its length is not a multiple of 2048) goes to a
+// small second kernel, so the hot loop has only full-block code.  Per block each
 // of its 128 threads owns sixteen contiguous elements: 16-byte streaming
 // loads of grad, param and both code arrays.  The kernel is bound by
 // instruction issue rather than by DRAM, so the loop is written to keep the
@@ -107,28 +109,158 @@ __device__ __forceinline__ float absmax4(float2 a, float2 b)
     return fmaxf(max3(fabsf(a.x), fabsf(a.y), fabsf(b.x)), fabsf(b.y));
 }
 
+// Shared-memory view of the staged tables and the reduction scratch.
+struct Smem8 {
+    const float* cs;
+    const float* cu;
+    const uint32_t* cell_s;
+    const uint32_t* cell_u;
+    uint2* red;                // [2][kW8]
+};
+
+__device__ __forceinline__ Smem8 stage_tables(const DevTables* tab, unsigned char* smem)
+{
+    const uint4* src = reinterpret_cast<const uint4*>(tab);
+    uint4* dst = reinterpret_cast<uint4*>(smem);
+    for (int i = threadIdx.x; i < static_cast<int>(sizeof(DevTables) / 16); i += kT8) dst[i] = src[i];
+    __syncthreads();
+    const DevTables* t = reinterpret_cast<const DevTables*>(smem);
+    return Smem8{t->cs, t->cu, t->cell_s, t->cell_u, reinterpret_cast<uint2*>(smem + sizeof(DevTables))};
+}
+
+// One 2048-element block of one tensor.  FULL: every thread owns sixteen
+// valid elements (the hot path: vector loads and stores only); otherwise the
+// block is the partial last block of its tensor.  `it` picks the half of the
+// double-buffered reduction scratch.
+template <bool SR, bool FULL>
+__device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int lb, int it, const Smem8& sm)
+{
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int64_t i0 = static_cast<int64_t>(lb) * kBlock + tid * kV8;
+    const int64_t rem = d.n - i0;                        // elements from i0 to the end
+    const float2 Mold = splat(d.ma[lb]);
+    const float2 Vold = splat(d.va[lb]);
+
+    Frag f;
+    if constexpr (FULL) {
+        const uint4 g0 = ld_stream16(d.g + i0), g1 = ld_stream16(d.g + i0 + 8);
+        const uint4 p0 = ld_stream16(d.p + i0), p1 = ld_stream16(d.p + i0 + 8);
+        const uint4 mq = ld_stream16(d.mq + i0);
+        const uint4 vq = ld_stream16(d.vq + i0);
+        f.g[0] = g0.x; f.g[1] = g0.y; f.g[2] = g0.z; f.g[3] = g0.w;
+        f.g[4] = g1.x; f.g[5] = g1.y; f.g[6] = g1.z; f.g[7] = g1.w;
+        f.p[0] = p0.x; f.p[1] = p0.y; f.p[2] = p0.z; f.p[3] = p0.w;
+        f.p[4] = p1.x; f.p[5] = p1.y; f.p[6] = p1.z; f.p[7] = p1.w;
+        f.mc[0] = mq.x; f.mc[1] = mq.y; f.mc[2] = mq.z; f.mc[3] = mq.w;
+        f.vc[0] = vq.x; f.vc[1] = vq.y; f.vc[2] = vq.z; f.vc[3] = vq.w;
+    } else {
+        load_ragged(d, i0, rem > 0 ? rem : 0, f);
+    }
+
+    // dequantize and update, two elements at a time
+    float2 m[8], v[8];
+    uint32_t po[8];
+    uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if constexpr (SR) {
+        const uint64_t E = d.e0 + static_cast<uint64_t>(i0);
+        draws8(E, 0u, s, r);
+        draws8(E + 8, 0u, s, r + 4);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t cw = f.mc[k >> 1], vw = f.vc[k >> 1];
+        const int b0 = (k & 1) * 2;
+        m[k] = __fmul2_rn(make_float2(sm.cs[byte_of(cw, b0)], sm.cs[byte_of(cw, b0 + 1)]), Mold);
+        v[k] = __fmul2_rn(make_float2(sm.cu[byte_of(vw, b0)], sm.cu[byte_of(vw, b0 + 1)]), Vold);
+        moments2(s, bf16x2(f.g[k]), m[k], v[k]);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float2 root = make_float2(__fsqrt_rn(v[k].x), __fsqrt_rn(v[k].y));
+        po[k] = round2<SR>(param2(s, bf16x2(f.p[k]), m[k], root), r[k]);
+    }
+
+    if constexpr (FULL) {
+        // the parameters do not wait for the block absmax: store them now
+        st_stream16(d.p + i0, make_uint4(po[0], po[1], po[2], po[3]));
+        st_stream16(d.p + i0 + 8, make_uint4(po[4], po[5], po[6], po[7]));
+    } else {
+        // padding elements do not count in the block absmax
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (2 * k >= rem) { m[k].x = 0.0f; v[k].x = 0.0f; }
+            if (2 * k + 1 >= rem) { m[k].y = 0.0f; v[k].y = 0.0f; }
+        }
+    }
+
+    // block absmax of the new moments
+    const float lm = fmaxf(fmaxf(absmax4(m[0], m[1]), absmax4(m[2], m[3])),
+                           fmaxf(absmax4(m[4], m[5]), absmax4(m[6], m[7])));
+    const float lv = fmaxf(fmaxf(absmax4(v[0], v[1]), absmax4(v[2], v[3])),
+                           fmaxf(absmax4(v[4], v[5]), absmax4(v[6], v[7])));
+    // non-negative floats order like their bit patterns
+    const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(lm));
+    const uint32_t wv = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(lv));
+    uint2* red = sm.red + (it & 1) * kW8;                // double-buffered: one barrier per block
+    if (lane == 0) red[warp] = make_uint2(wm, wv);
+    __syncthreads();
+    const uint2 t = lane < kW8 ? red[lane] : make_uint2(0u, 0u);
+    const float M = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, t.x));
+    const float V = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, t.y));
+
+    // requantize against the new absmax: scale by RN(1/absmax), look up
+    uint32_t mo[4], vo[4];
+    if (M > 0.0f) {
+        const float im = __frcp_rn(M);
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            mo[k >> 1] = pack4(code_signed_scaled(m[k].x, im, sm.cell_s), code_signed_scaled(m[k].y, im, sm.cell_s),
+                               code_signed_scaled(m[k + 1].x, im, sm.cell_s),
+                               code_signed_scaled(m[k + 1].y, im, sm.cell_s));
+        }
+    } else {
+        mo[0] = mo[1] = mo[2] = mo[3] = 0x7F7F7F7Fu;
+    }
+    if (V > 0.0f) {
+        const float iv = __frcp_rn(V);
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            vo[k >> 1] = pack4(code_unsigned_scaled(v[k].x, iv, sm.cell_u), code_unsigned_scaled(v[k].y, iv, sm.cell_u),
+                               code_unsigned_scaled(v[k + 1].x, iv, sm.cell_u),
+                               code_unsigned_scaled(v[k + 1].y, iv, sm.cell_u));
+        }
+    } else {
+        vo[0] = vo[1] = vo[2] = vo[3] = 0u;
+    }
+
+    if constexpr (FULL) {
+        st_stream16(d.mq + i0, make_uint4(mo[0], mo[1], mo[2], mo[3]));
+        st_stream16(d.vq + i0, make_uint4(vo[0], vo[1], vo[2], vo[3]));
+    } else if (rem > 0) {
+        store_ragged(d, i0, rem, po, mo, vo);
+    }
+    if (tid == 0) {
+        d.ma[lb] = M;
+        d.va[lb] = V;
+    }
+}
+
+__device__ __forceinline__ bool is_partial(const Desc8& d, int lb)
+{
+    return static_cast<int64_t>(lb + 1) * kBlock > d.n;
+}
+
+// The hot kernel: every full block of the launch's list.  Partial last blocks
+// are left to step8_tail_kernel, so this loop carries no ragged-tail code.
 template <bool SR>
 __global__ void __launch_bounds__(kT8, 7) step8_kernel(const __grid_constant__ Step8Args a)
 {
     extern __shared__ __align__(16) unsigned char smem[];
-    const DevTables* tabs = reinterpret_cast<const DevTables*>(smem);
-    const float* s_cs = tabs->cs;
-    const float* s_cu = tabs->cu;
-    const uint32_t* s_cell_s = tabs->cell_s;
-    const uint32_t* s_cell_u = tabs->cell_u;
-    uint2* s_red = reinterpret_cast<uint2*>(smem + sizeof(DevTables));   // [2][kW8]
+    const Smem8 sm = stage_tables(a.tab, smem);
 
-    {
-        const uint4* src = reinterpret_cast<const uint4*>(a.tab);
-        uint4* dst = reinterpret_cast<uint4*>(smem);
-        for (int i = threadIdx.x; i < static_cast<int>(sizeof(DevTables) / 16); i += kT8) dst[i] = src[i];
-    }
-    __syncthreads();
-
-    const Scalars& s = a.s;
     const int tid = threadIdx.x;
-    const int lane = tid & 31;
-    const int warp = tid >> 5;
     const int begin = static_cast<int>((static_cast<int64_t>(blockIdx.x) * a.nblocks) / gridDim.x);
     const int end = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * a.nblocks) / gridDim.x);
     int ti = begin < end ? find_tensor(a.blk_start, a.nt, begin) : 0;
@@ -143,7 +275,7 @@ __global__ void __launch_bounds__(kT8, 7) step8_kernel(const __grid_constant__ S
         }
     }
 
-    for (int gb = begin, it = 0; gb < end; ++gb, ++it) {
+    for (int gb = begin, it = 0; gb < end; ++gb) {
         if (tid == 0 && pb < end) {
             while (pb >= a.blk_start[tp + 1]) ++tp;
             prefetch_block(a.d[tp], pb - a.blk_start[tp]);
@@ -152,115 +284,22 @@ __global__ void __launch_bounds__(kT8, 7) step8_kernel(const __grid_constant__ S
         while (gb >= a.blk_start[ti + 1]) ++ti;
         const Desc8& d = a.d[ti];
         const int lb = gb - a.blk_start[ti];
-        const int64_t i0 = static_cast<int64_t>(lb) * kBlock + tid * kV8;
-        const int64_t rem = d.n - i0;                    // elements from i0 to the end
-        const bool full = rem >= kV8;
-        const float2 Mold = splat(d.ma[lb]);
-        const float2 Vold = splat(d.va[lb]);
-
-        Frag f;
-        if (full) {
-            const uint4 g0 = ld_stream16(d.g + i0), g1 = ld_stream16(d.g + i0 + 8);
-            const uint4 p0 = ld_stream16(d.p + i0), p1 = ld_stream16(d.p + i0 + 8);
-            const uint4 mq = ld_stream16(d.mq + i0);
-            const uint4 vq = ld_stream16(d.vq + i0);
-            f.g[0] = g0.x; f.g[1] = g0.y; f.g[2] = g0.z; f.g[3] = g0.w;
-            f.g[4] = g1.x; f.g[5] = g1.y; f.g[6] = g1.z; f.g[7] = g1.w;
-            f.p[0] = p0.x; f.p[1] = p0.y; f.p[2] = p0.z; f.p[3] = p0.w;
-            f.p[4] = p1.x; f.p[5] = p1.y; f.p[6] = p1.z; f.p[7] = p1.w;
-            f.mc[0] = mq.x; f.mc[1] = mq.y; f.mc[2] = mq.z; f.mc[3] = mq.w;
-            f.vc[0] = vq.x; f.vc[1] = vq.y; f.vc[2] = vq.z; f.vc[3] = vq.w;
-        } else {
-            load_ragged(d, i0, rem > 0 ? rem : 0, f);
-        }
-
-        // dequantize and update, two elements at a time
-        float2 m[8], v[8];
-        uint32_t po[8];
-        uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-        if constexpr (SR) {
-            const uint64_t E = d.e0 + static_cast<uint64_t>(i0);
-            draws8(E, 0u, s, r);
-            draws8(E + 8, 0u, s, r + 4);
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const uint32_t cw = f.mc[k >> 1], vw = f.vc[k >> 1];
-            const int b0 = (k & 1) * 2;
-            m[k] = __fmul2_rn(make_float2(s_cs[byte_of(cw, b0)], s_cs[byte_of(cw, b0 + 1)]), Mold);
-            v[k] = __fmul2_rn(make_float2(s_cu[byte_of(vw, b0)], s_cu[byte_of(vw, b0 + 1)]), Vold);
-            moments2(s, bf16x2(f.g[k]), m[k], v[k]);
-        }
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float2 root = make_float2(__fsqrt_rn(v[k].x), __fsqrt_rn(v[k].y));
-            po[k] = round2<SR>(param2(s, bf16x2(f.p[k]), m[k], root), r[k]);
-        }
-
-        // the parameters do not wait for the block absmax: store them now
-        if (full) {
-            st_stream16(d.p + i0, make_uint4(po[0], po[1], po[2], po[3]));
-            st_stream16(d.p + i0 + 8, make_uint4(po[4], po[5], po[6], po[7]));
-        }
-
-        // block absmax of the new moments (padding elements do not count)
-        if (!full) {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                if (2 * k >= rem) { m[k].x = 0.0f; v[k].x = 0.0f; }
-                if (2 * k + 1 >= rem) { m[k].y = 0.0f; v[k].y = 0.0f; }
-            }
-        }
-        const float lm = fmaxf(fmaxf(absmax4(m[0], m[1]), absmax4(m[2], m[3])),
-                               fmaxf(absmax4(m[4], m[5]), absmax4(m[6], m[7])));
-        const float lv = fmaxf(fmaxf(absmax4(v[0], v[1]), absmax4(v[2], v[3])),
-                               fmaxf(absmax4(v[4], v[5]), absmax4(v[6], v[7])));
-        // non-negative floats order like their bit patterns
-        const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(lm));
-        const uint32_t wv = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(lv));
-        uint2* red = s_red + (it & 1) * kW8;             // double-buffered: one barrier per block
-        if (lane == 0) red[warp] = make_uint2(wm, wv);
-        __syncthreads();
-        const uint2 t = lane < kW8 ? red[lane] : make_uint2(0u, 0u);
-        const float M = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, t.x));
-        const float V = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, t.y));
-
-        // requantize against the new absmax: scale by RN(1/absmax), look up
-        uint32_t mo[4], vo[4];
-        if (M > 0.0f) {
-            const float im = __frcp_rn(M);
-#pragma unroll
-            for (int k = 0; k < 8; k += 2) {
-                mo[k >> 1] = pack4(code_signed_scaled(m[k].x, im, s_cell_s), code_signed_scaled(m[k].y, im, s_cell_s),
-                                   code_signed_scaled(m[k + 1].x, im, s_cell_s),
-                                   code_signed_scaled(m[k + 1].y, im, s_cell_s));
-            }
-        } else {
-            mo[0] = mo[1] = mo[2] = mo[3] = 0x7F7F7F7Fu;
-        }
-        if (V > 0.0f) {
-            const float iv = __frcp_rn(V);
-#pragma unroll
-            for (int k = 0; k < 8; k += 2) {
-                vo[k >> 1] = pack4(code_unsigned_scaled(v[k].x, iv, s_cell_u), code_unsigned_scaled(v[k].y, iv, s_cell_u),
-                                   code_unsigned_scaled(v[k + 1].x, iv, s_cell_u),
-                                   code_unsigned_scaled(v[k + 1].y, iv, s_cell_u));
-            }
-        } else {
-            vo[0] = vo[1] = vo[2] = vo[3] = 0u;
-        }
-
-        if (full) {
-            st_stream16(d.mq + i0, make_uint4(mo[0], mo[1], mo[2], mo[3]));
-            st_stream16(d.vq + i0, make_uint4(vo[0], vo[1], vo[2], vo[3]));
-        } else if (rem > 0) {
-            store_ragged(d, i0, rem, po, mo, vo);
-        }
-        if (tid == 0) {
-            d.ma[lb] = M;
-            d.va[lb] = V;
-        }
+        if (is_partial(d, lb)) continue;                 // uniform across the CTA
+        block_step<SR, true>(a.s, d, lb, it++, sm);
     }
+}
+
+// Partial last blocks: one CTA per tensor of the launch, idle unless the
+// tensor's length is not a multiple of 2048.
+template <bool SR>
+__global__ void __launch_bounds__(kT8) step8_tail_kernel(const __grid_constant__ Step8Args a)
+{
+    const Desc8& d = a.d[blockIdx.x];
+    const int lb = static_cast<int>((d.n - 1) / kBlock);
+    if (!is_partial(d, lb)) return;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const Smem8 sm = stage_tables(a.tab, smem);
+    block_step<SR, false>(a.s, d, lb, 0, sm);
 }
 
 // fp32-state path: one CTA per tensor (numel < 4096 = 512 threads x 8).
@@ -299,18 +338,22 @@ __global__ void __launch_bounds__(kSmallThreads) step32_kernel(const __grid_cons
 }
 
 template <bool SR>
-cudaError_t launch_step8_t(const Step8Args& a, cudaStream_t st)
+cudaError_t launch_step8_t(const Step8Args& a, bool has_partial, cudaStream_t st)
 {
     static int full = 0;
     if (full == 0) {
         const void* k = reinterpret_cast<const void*>(step8_kernel<SR>);
         cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
         if (e != cudaSuccess) return e;
+        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(step8_tail_kernel<SR>),
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+        if (e != cudaSuccess) return e;
         full = resident_ctas(k, kT8, kSmemBytes);
         if (full <= 0) return cudaErrorUnknown;
     }
     const int grid = a.nblocks < full ? a.nblocks : full;
     if (grid > 0) step8_kernel<SR><<<grid, kT8, kSmemBytes, st>>>(a);
+    if (has_partial && a.nt > 0) step8_tail_kernel<SR><<<a.nt, kT8, kSmemBytes, st>>>(a);
     return cudaGetLastError();
 }
 
@@ -328,7 +371,9 @@ int resident_ctas(const void* kernel, int threads, size_t smem)
 
 cudaError_t launch_step8(const Step8Args& a, cudaStream_t st)
 {
-    return a.s.sr ? launch_step8_t<true>(a, st) : launch_step8_t<false>(a, st);
+    bool has_partial = false;
+    for (int i = 0; i < a.nt; ++i) has_partial = has_partial || (a.d[i].n % kBlock) != 0;
+    return a.s.sr ? launch_step8_t<true>(a, has_partial, st) : launch_step8_t<false>(a, has_partial, st);
 }
 
 cudaError_t launch_step32(const Step32Args& a, cudaStream_t st)
