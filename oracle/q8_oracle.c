@@ -30,6 +30,10 @@
  *        TL;DR and abstract (BF16-AdamW-SR, shared randomness).
  *  Philox4x32-10 follows Salmon, Moraes, Dror and Shaw, "Parallel Random
  *  Numbers: As Easy as 1, 2, 3" (SC'11), section on the Philox family.
+ *  The one-state optimizers follow their published definitions: SGD with
+ *  momentum as in PyTorch's SGD (dampening 0, weight decay added to the
+ *  gradient) and Lion from Chen et al., "Symbolic Discovery of Optimization
+ *  Algorithms" (2023), Algorithm 2 (decoupled weight decay).
  *
  * Readings taken where the pages are silent are listed with each function.
  *
@@ -468,6 +472,103 @@ int q8o_adamw_bf16_sr_step(const q8o_tensor16* list, int n, const q8o_hparams* h
         const q8o_tensor16* t = &list[i];
         uint64_t E0 = t->philox_offset >= 0 ? (uint64_t)t->philox_offset : running;
         q8o_adamw_bf16_tensor(t, E0, hp);
+        running += (uint64_t)t->numel;
+    }
+    return 0;
+}
+
+/* ------------------------------------------------------------------------ */
+/* One-state optimizers with an 8-bit blockwise first moment and the same   */
+/* SR parameter write.  [BW] introduction: optimizer states of Adam and     */
+/* Momentum; [SR] motivation: 8-bit Lion.  fp32, each x*y + z fused:        */
+/*   Momentum: d = fma(wd, p, g); m = fma(mu, m, d); p = fma(-lr, m, p)     */
+/*   Lion:     c = fma(b1, m, (1-b1)*g); u = sign(c) (0 for c = 0);         */
+/*             p = fma(-lr, u, p*(1 - lr*wd)); m = fma(b2, m, (1-b2)*g)     */
+/* Hyper-parameters travel in q8o_hparams: momentum uses beta1 as mu; eps   */
+/* is unused.                                                               */
+/* ------------------------------------------------------------------------ */
+
+enum { Q8O_MOMENTUM = 0, Q8O_LION = 1 };
+
+typedef struct { float lr_neg, a, oma, b, omb, decay, wd; } q8o_scalars1;
+
+void q8o_step_scalars1(int opt, const q8o_hparams* hp, q8o_scalars1* s)
+{
+    s->lr_neg = (float)(-hp->lr);
+    s->a = (float)hp->beta1;
+    s->oma = (float)(1.0 - hp->beta1);
+    s->b = (float)hp->beta2;
+    s->omb = (float)(1.0 - hp->beta2);
+    s->decay = (float)(1.0 - hp->lr * hp->weight_decay);
+    s->wd = (float)hp->weight_decay;
+    (void)opt;
+}
+
+/* One element: returns the new fp32 parameter, updates *m in place. */
+float q8o_onestate_element(int opt, const q8o_scalars1* s, float g, float p, float* m)
+{
+    if (opt == Q8O_MOMENTUM) {
+        float d = fmaf(s->wd, p, g);
+        float mn = fmaf(s->a, *m, d);
+        *m = mn;
+        return fmaf(s->lr_neg, mn, p);
+    }
+    float c = fmaf(s->a, *m, s->oma * g);
+    float u = c > 0.0f ? 1.0f : (c < 0.0f ? -1.0f : 0.0f);
+    float pn = fmaf(s->lr_neg, u, p * s->decay);
+    *m = fmaf(s->b, *m, s->omb * g);
+    return pn;
+}
+
+/* 8-bit state, one tensor (m_codes / m_absmax; the v fields are unused). */
+void q8o_onestate8bit_tensor(int opt, const q8o_tensor8* t, uint64_t E0, const q8o_hparams* hp)
+{
+    q8o_scalars1 s;
+    q8o_step_scalars1(opt, hp, &s);
+    float cs[256], mid_s[255];
+    q8o_codebook(Q8O_SIGNED, cs);
+    q8o_midpoints(Q8O_SIGNED, mid_s);
+    float mb[Q8O_BLOCK];
+    for (int64_t b = 0; b * Q8O_BLOCK < t->numel; ++b) {
+        int64_t base = b * Q8O_BLOCK;
+        int64_t len = t->numel - base;
+        if (len > Q8O_BLOCK) len = Q8O_BLOCK;
+        float Mold = t->m_absmax[b];
+        for (int64_t i = 0; i < len; ++i) {
+            int64_t e = base + i;
+            float m = cs[t->m_codes[e]] * Mold;
+            float g = q8o_bf16_to_f32(t->grad[e]);
+            float p = q8o_bf16_to_f32(t->param[e]);
+            float pn = q8o_onestate_element(opt, &s, g, p, &m);
+            t->param[e] = round_param(hp, pn, 0, E0 + (uint64_t)e);
+            mb[i] = m;
+        }
+        quantize_block(mid_s, q8o_zero_code(Q8O_SIGNED), mb, len, t->m_codes + base, t->m_absmax + b);
+    }
+}
+
+void q8o_onestate32_tensor(int opt, const q8o_tensor8* t, uint64_t E0, const q8o_hparams* hp)
+{
+    q8o_scalars1 s;
+    q8o_step_scalars1(opt, hp, &s);
+    for (int64_t e = 0; e < t->numel; ++e) {
+        float m = t->m32[e];
+        float g = q8o_bf16_to_f32(t->grad[e]);
+        float p = q8o_bf16_to_f32(t->param[e]);
+        float pn = q8o_onestate_element(opt, &s, g, p, &m);
+        t->param[e] = round_param(hp, pn, 0, E0 + (uint64_t)e);
+        t->m32[e] = m;
+    }
+}
+
+int q8o_onestate_sr_step(int opt, const q8o_tensor8* list, int n, const q8o_hparams* hp)
+{
+    uint64_t running = 0;
+    for (int i = 0; i < n; ++i) {
+        const q8o_tensor8* t = &list[i];
+        uint64_t E0 = t->philox_offset >= 0 ? (uint64_t)t->philox_offset : running;
+        if (t->m_codes) q8o_onestate8bit_tensor(opt, t, E0, hp);
+        else q8o_onestate32_tensor(opt, t, E0, hp);
         running += (uint64_t)t->numel;
     }
     return 0;

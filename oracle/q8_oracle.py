@@ -50,6 +50,13 @@ def lib():
         L.q8o_adamw_bf16_tensor.argtypes = [C.POINTER(Tensor16), C.c_uint64, C.POINTER(HParams)]
         L.q8o_adamw8bit_sr_step.argtypes = [C.POINTER(Tensor8), C.c_int, C.POINTER(HParams)]
         L.q8o_adamw_bf16_sr_step.argtypes = [C.POINTER(Tensor16), C.c_int, C.POINTER(HParams)]
+        L.q8o_step_scalars1.argtypes = [C.c_int, C.POINTER(HParams), C.POINTER(Scalars1)]
+        L.q8o_onestate_element.argtypes = [C.c_int, C.POINTER(Scalars1), C.c_float, C.c_float,
+                                           C.POINTER(C.c_float)]
+        L.q8o_onestate_element.restype = C.c_float
+        L.q8o_onestate8bit_tensor.argtypes = [C.c_int, C.POINTER(Tensor8), C.c_uint64, C.POINTER(HParams)]
+        L.q8o_onestate32_tensor.argtypes = [C.c_int, C.POINTER(Tensor8), C.c_uint64, C.POINTER(HParams)]
+        L.q8o_onestate_sr_step.argtypes = [C.c_int, C.POINTER(Tensor8), C.c_int, C.POINTER(HParams)]
         _lib = L
     return _lib
 
@@ -63,6 +70,13 @@ class HParams(C.Structure):
 class Scalars(C.Structure):
     _fields_ = [(n, C.c_float) for n in
                 ("b1", "omb1", "b2", "omb2", "eps_t", "step_size", "decay")]
+
+
+class Scalars1(C.Structure):
+    _fields_ = [(n, C.c_float) for n in ("lr_neg", "a", "oma", "b", "omb", "decay", "wd")]
+
+
+MOMENTUM, LION = 0, 1
 
 
 class Tensor8(C.Structure):
@@ -264,3 +278,48 @@ def adamw_bf16_tensor(state, E0, hp):
 
 def lib_path():
     return os.path.abspath(_build.LIB)
+
+
+def step_scalars1(opt, hp):
+    s = Scalars1()
+    lib().q8o_step_scalars1(opt, C.byref(hp), C.byref(s))
+    return s
+
+
+def onestate_element(opt, s, g, p, m):
+    """One element of Momentum / Lion; returns (p_new, m_new) as float32."""
+    mm = C.c_float(float(np.float32(m)))
+    pn = lib().q8o_onestate_element(opt, C.byref(s), float(np.float32(g)), float(np.float32(p)), C.byref(mm))
+    return np.float32(pn), np.float32(mm.value)
+
+
+def onestate_sr_step(opt, states, hp):
+    """Momentum / Lion step over a list of State8 (m only; v fields unused)."""
+    arr = (Tensor8 * len(states))(*[s.struct() for s in states])
+    lib().q8o_onestate_sr_step(opt, arr, len(states), C.byref(hp))
+
+
+def onestate8bit_tensor(opt, state, E0, hp):
+    if state.m_codes is None or state.m_absmax is None:
+        raise ValueError("onestate8bit_tensor needs m_codes and m_absmax")
+    t = state.struct()
+    lib().q8o_onestate8bit_tensor(opt, C.byref(t), E0, C.byref(hp))
+
+
+def onestate32_tensor(opt, state, E0, hp):
+    if state.m32 is None:
+        raise ValueError("onestate32_tensor needs m32")
+    t = state.struct()
+    lib().q8o_onestate32_tensor(opt, C.byref(t), E0, C.byref(hp))
+
+
+def zeros_onestate(param, grad, philox_offset=-1, eight_bit=None):
+    """Fresh one-state (m only) state."""
+    n = param.size
+    if eight_bit is None:
+        eight_bit = n >= SMALL
+    if eight_bit:
+        nb = (n + BLOCK - 1) // BLOCK
+        return State8(param, grad, m_codes=np.full(n, zero_code(SIGNED), np.uint8),
+                      m_absmax=np.zeros(nb, np.float32), philox_offset=philox_offset)
+    return State8(param, grad, m32=np.zeros(n, np.float32), philox_offset=philox_offset)
