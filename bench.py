@@ -44,6 +44,8 @@ def parse():
                     help="replace the workload by one flat tensor of this many params (profiling)")
     ap.add_argument("--flat-state", default="8bit", choices=["8bit", "bf16"],
                     help="optimizer state of the --flat tensor")
+    ap.add_argument("--optimizer", default="adamw", choices=["adamw", "momentum", "lion"],
+                    help="8-bit-state optimizer of the step (adamw is the headline)")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
@@ -71,18 +73,19 @@ def workload(args):
     return W.WORKLOADS[args.workload]
 
 
-def algorithmic_bytes(wl):
+def algorithmic_bytes(wl, moments=2):
     """Bytes the step must move: 8-bit path 10 B/param (grad 2, param 2+2,
     codes 1+1 each way) + 16 B per block (two absmax read and written);
-    fp32-state path 22 B/param; BF16-state path 14 B/param."""
+    fp32-state path 22 B/param; BF16-state path 14 B/param.  With one moment
+    (Momentum, Lion): 8 B/param + 8 B/block, fp32 state 14 B/param."""
     total = 0
     for t in wl.tensors:
         if wl.state == "bf16":
             total += 14 * t.numel
         elif t.numel >= 4096:
-            total += 10 * t.numel + 16 * ((t.numel + BLOCK - 1) // BLOCK)
+            total += (4 + 3 * moments) * t.numel + 8 * moments * ((t.numel + BLOCK - 1) // BLOCK)
         else:
-            total += 22 * t.numel
+            total += (6 + 8 * moments) * t.numel
     return total
 
 
@@ -264,18 +267,26 @@ def main():
     q8.q8_prepare_device()
     params = W.init_params(wl, device)
     grads = W.make_grads(wl, 1, device)
+    moments = 2 if args.optimizer == "adamw" else 1
     if wl.state == "bf16":
         states = [q8.Tensor16(p, g, torch.zeros_like(p), torch.zeros_like(p)) for p, g in zip(params, grads)]
         packed = q8.pack_tensor16(states)
         step_fn = q8.adamw_bf16_sr_step
     else:
-        states = [q8.Tensor8.zeros_like(p, g) for p, g in zip(params, grads)]
+        states = [q8.Tensor8.zeros_like(p, g, moments=moments) for p, g in zip(params, grads)]
         packed = q8.pack_tensor8(states)
-        step_fn = q8.adamw8bit_sr_step
+        step_fn = {"adamw": q8.adamw8bit_sr_step, "momentum": q8.momentum8bit_sr_step,
+                   "lion": q8.lion8bit_sr_step}[args.optimizer]
     numel = wl.numel
     h = dict(wl.hp)
 
     def hp(t):
+        if args.optimizer == "momentum":
+            return q8.momentum_hparams(lr=h["lr"], momentum=h["beta1"], weight_decay=h["weight_decay"],
+                                       step=t, seed=wl.philox_seed)
+        if args.optimizer == "lion":
+            return q8.lion_hparams(lr=h["lr"], beta1=h["beta1"], beta2=0.99, weight_decay=h["weight_decay"],
+                                   step=t, seed=wl.philox_seed)
         return q8.hparams(lr=h["lr"], beta1=h["beta1"], beta2=h["beta2"], eps=h["eps"],
                           weight_decay=h["weight_decay"], step=t, seed=wl.philox_seed)
 
@@ -314,11 +325,11 @@ def main():
 
     # roofline of the dominant kernel (the fused step kernel: one launch per step here)
     peak, peak_kind = load_peaks()
-    abytes = algorithmic_bytes(wl)
+    abytes = algorithmic_bytes(wl, moments)
     nl = launches_per_step(wl)
     mean_ms = statistics.mean(per)
     achieved = abytes / (mean_ms / 1e3) / 1e9
-    kernel = "step16_kernel" if wl.state == "bf16" else "step8_kernel"
+    kernel = "step16_kernel" if wl.state == "bf16" else ("step8_kernel" if moments == 2 else "step1_kernel")
     traffic = traffic_per_launch(kernel, numel / nl) if nl == 1 else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": kernel,
@@ -328,12 +339,12 @@ def main():
     # end to end through the public API: grads in from pinned host memory,
     # step, updated params back to pinned host memory, every step
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.optimizer == "adamw":
         e2e = run_e2e(args, wl, states, step_fn, hp, t, device, world, barrier)
         t += args.e2e_steps + 1
 
     cpu = None
-    if not args.no_cpu_baseline and rank == 0:
+    if not args.no_cpu_baseline and rank == 0 and args.optimizer == "adamw":
         n, dt = oracle_sample_time(wl, args.cpu_blocks)
         cpu = {"value": n / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": "%d seeded 2048-blocks (%d params) of %s, one step, single-threaded C oracle"
@@ -344,7 +355,7 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": wl.name, "params": numel, "tensors": len(wl.tensors),
+            "config": {"workload": wl.name, "optimizer": args.optimizer, "params": numel, "tensors": len(wl.tensors),
                        "blocks": wl.blocks(), "state": wl.state,
                        "bytes_per_step": abytes, "gbs": abytes / (ms_per_step / 1e3) / 1e9,
                        "l2": "inputs larger than L2 (%.1f GB moved per step, no flush)" % (abytes / 1e9),

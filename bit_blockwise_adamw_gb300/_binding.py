@@ -25,8 +25,8 @@ _STATUS = {-1: "Q8_ERR_NULL", -2: "Q8_ERR_SIZE", -3: "Q8_ERR_ALIGN", -4: "Q8_ERR
 
 # every symbol the header declares
 EXPORTS = ("q8_codebook_init", "q8_blockwise_quantize", "q8_blockwise_dequantize",
-           "adamw8bit_sr_step", "adamw_bf16_sr_step", "q8_philox_fill",
-           "q8_prepare_device", "q8_last_error", "q8_abi_version")
+           "adamw8bit_sr_step", "adamw_bf16_sr_step", "momentum8bit_sr_step", "lion8bit_sr_step",
+           "q8_philox_fill", "q8_prepare_device", "q8_last_error", "q8_abi_version")
 
 
 class Q8Error(RuntimeError):
@@ -42,6 +42,18 @@ class HParams(C.Structure):
     _fields_ = [("lr", C.c_double), ("beta1", C.c_double), ("beta2", C.c_double),
                 ("eps", C.c_double), ("weight_decay", C.c_double),
                 ("step", C.c_int64), ("seed", C.c_uint64), ("sr", C.c_int32)]
+
+
+class MomentumHParams(C.Structure):
+    """q8_momentum_hparams."""
+    _fields_ = [("lr", C.c_double), ("momentum", C.c_double), ("weight_decay", C.c_double),
+                ("step", C.c_int64), ("seed", C.c_uint64), ("sr", C.c_int32)]
+
+
+class LionHParams(C.Structure):
+    """q8_lion_hparams."""
+    _fields_ = [("lr", C.c_double), ("beta1", C.c_double), ("beta2", C.c_double),
+                ("weight_decay", C.c_double), ("step", C.c_int64), ("seed", C.c_uint64), ("sr", C.c_int32)]
 
 
 class _Tensor8(C.Structure):
@@ -78,6 +90,8 @@ def load_library(path: Optional[str] = None):
     L.q8_blockwise_dequantize.argtypes = [P, P, P, C.c_int64, C.c_int, S]
     L.adamw8bit_sr_step.argtypes = [C.POINTER(_Tensor8), C.c_int, C.POINTER(HParams), S]
     L.adamw_bf16_sr_step.argtypes = [C.POINTER(_Tensor16), C.c_int, C.POINTER(HParams), S]
+    L.momentum8bit_sr_step.argtypes = [C.POINTER(_Tensor8), C.c_int, C.POINTER(MomentumHParams), S]
+    L.lion8bit_sr_step.argtypes = [C.POINTER(_Tensor8), C.c_int, C.POINTER(LionHParams), S]
     L.q8_philox_fill.argtypes = [C.c_uint64, C.c_uint32, C.c_uint32, C.c_uint64, C.c_int64, P, S]
     L.q8_prepare_device.argtypes = []
     L.q8_last_error.argtypes = []
@@ -113,6 +127,14 @@ def _stream(stream):
 
 def hparams(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=1, seed=0, sr=1):
     return HParams(lr, beta1, beta2, eps, weight_decay, step, seed, sr)
+
+
+def momentum_hparams(lr=1e-2, momentum=0.9, weight_decay=0.0, step=1, seed=0, sr=1):
+    return MomentumHParams(lr, momentum, weight_decay, step, seed, sr)
+
+
+def lion_hparams(lr=1e-4, beta1=0.9, beta2=0.99, weight_decay=0.0, step=1, seed=0, sr=1):
+    return LionHParams(lr, beta1, beta2, weight_decay, step, seed, sr)
 
 
 # ---------------------------------------------------------------- entry points
@@ -176,18 +198,23 @@ class Tensor8:
     philox_offset: int = -1
 
     @classmethod
-    def zeros_like(cls, param: torch.Tensor, grad: Optional[torch.Tensor] = None, philox_offset=-1):
-        """Fresh (all-zero) state for `param` on its device."""
+    def zeros_like(cls, param: torch.Tensor, grad: Optional[torch.Tensor] = None, philox_offset=-1,
+                   moments: int = 2):
+        """Fresh (all-zero) state for `param` on its device: first and second
+        moment (AdamW) or, with moments=1, the first only (Momentum, Lion)."""
         n = param.numel()
         dev = param.device
+        two = moments == 2
         if n >= SMALL_NUMEL:
             nb = (n + BLOCK - 1) // BLOCK
             return cls(param, grad, torch.full((n,), 127, dtype=torch.uint8, device=dev),
-                       torch.zeros(n, dtype=torch.uint8, device=dev),
+                       torch.zeros(n, dtype=torch.uint8, device=dev) if two else None,
                        torch.zeros(nb, dtype=torch.float32, device=dev),
-                       torch.zeros(nb, dtype=torch.float32, device=dev), philox_offset=philox_offset)
+                       torch.zeros(nb, dtype=torch.float32, device=dev) if two else None,
+                       philox_offset=philox_offset)
         return cls(param, grad, m32=torch.zeros(n, dtype=torch.float32, device=dev),
-                   v32=torch.zeros(n, dtype=torch.float32, device=dev), philox_offset=philox_offset)
+                   v32=torch.zeros(n, dtype=torch.float32, device=dev) if two else None,
+                   philox_offset=philox_offset)
 
     def slice(self, start: int, count: int, philox_offset: int):
         """Block-aligned slice [start, start + count) of this tensor with the
@@ -196,9 +223,9 @@ class Tensor8:
         assert start % BLOCK == 0 and 0 <= start and start + count <= self.param.numel()
         b0, b1 = start // BLOCK, (start + count + BLOCK - 1) // BLOCK
         sl = slice(start, start + count)
-        return Tensor8(self.param[sl], None if self.grad is None else self.grad[sl],
-                       self.m_codes[sl], self.v_codes[sl], self.m_absmax[b0:b1], self.v_absmax[b0:b1],
-                       philox_offset=philox_offset)
+        opt = lambda t, s: None if t is None else t[s]
+        return Tensor8(self.param[sl], opt(self.grad, sl), self.m_codes[sl], opt(self.v_codes, sl),
+                       self.m_absmax[b0:b1], opt(self.v_absmax, slice(b0, b1)), philox_offset=philox_offset)
 
     def _struct(self):
         assert self.param.dtype == torch.bfloat16 and self.grad.dtype == torch.bfloat16
@@ -244,3 +271,16 @@ def adamw_bf16_sr_step(tensors, hp: HParams, stream=None) -> None:
     """BF16-state AdamW + SR step over a list of Tensor16 (or a packed list)."""
     arr = tensors if isinstance(tensors, C.Array) else pack_tensor16(tensors)
     _check("adamw_bf16_sr_step", load_library().adamw_bf16_sr_step(arr, len(arr), C.byref(hp), _stream(stream)))
+
+
+def momentum8bit_sr_step(tensors, hp: MomentumHParams, stream=None) -> None:
+    """8-bit SGD-with-momentum step with SR parameter write over a list of
+    Tensor8 holding first-moment state only (see Tensor8.zeros_like(moments=1))."""
+    arr = tensors if isinstance(tensors, C.Array) else pack_tensor8(tensors)
+    _check("momentum8bit_sr_step", load_library().momentum8bit_sr_step(arr, len(arr), C.byref(hp), _stream(stream)))
+
+
+def lion8bit_sr_step(tensors, hp: LionHParams, stream=None) -> None:
+    """8-bit Lion step with SR parameter write (first-moment state only)."""
+    arr = tensors if isinstance(tensors, C.Array) else pack_tensor8(tensors)
+    _check("lion8bit_sr_step", load_library().lion8bit_sr_step(arr, len(arr), C.byref(hp), _stream(stream)))

@@ -74,11 +74,137 @@ int check_offset(int64_t e0, int64_t numel, int i)
     return Q8_OK;
 }
 
+int check_common(double lr, double wd, int64_t step, int32_t sr)
+{
+    if (!std::isfinite(lr) || !std::isfinite(wd)) return fail(Q8_ERR_ARG, "hyper-parameters must be finite");
+    if (lr < 0.0) return fail(Q8_ERR_ARG, "lr must be >= 0");
+    if (wd < 0.0) return fail(Q8_ERR_ARG, "weight_decay must be >= 0");
+    if (step < 1 || step > Q8_MAX_STEP) return fail(Q8_ERR_ARG, "step must lie in [1, 2^31)");
+    if (sr != 0 && sr != 1) return fail(Q8_ERR_ARG, "sr must be 0 or 1");
+    return Q8_OK;
+}
+
+int check_beta(double b, const char* what)
+{
+    if (!std::isfinite(b) || b < 0.0 || b >= 1.0) return fail(Q8_ERR_ARG, std::string(what) + " must lie in [0, 1)");
+    return Q8_OK;
+}
+
+// Momentum / Lion over a list: validate, then launch chunks of up to kMaxList
+// entries (8-bit state on step1_kernel, fp32 state on step1_32_kernel).
+int onestate_step(int opt, const q8_tensor8* list, int ntensors, const q8::Scalars1& s, cudaStream_t stream)
+{
+    if (ntensors < 0) return fail(Q8_ERR_SIZE, "ntensors must be >= 0");
+    if (ntensors > 0 && !list) return fail(Q8_ERR_NULL, "list is NULL");
+    int64_t running = 0;
+    int rc;
+    for (int i = 0; i < ntensors; ++i) {
+        const q8_tensor8& t = list[i];
+        if (t.numel < 0 || t.numel >= kMaxNumel) return fail(Q8_ERR_SIZE, at("numel must lie in [0, 2^40)", i));
+        const int64_t e0 = t.philox_offset >= 0 ? t.philox_offset : running;
+        running += t.numel;
+        if (t.numel == 0) continue;
+        if ((rc = check_offset(e0, t.numel, i)) != Q8_OK) return rc;
+        if (!t.param || !t.grad) return fail(Q8_ERR_NULL, at("param and grad must be non-NULL", i));
+        if (!aligned(t.param, 16) || !aligned(t.grad, 16))
+            return fail(Q8_ERR_ALIGN, at("param and grad must be 16-byte aligned", i));
+        if (t.v_codes || t.v_absmax || t.v32)
+            return fail(Q8_ERR_ARG, at("one-state optimizers take no second-moment state", i));
+        if (t.m_codes) {
+            if (t.m32) return fail(Q8_ERR_ARG, at("an entry carries either 8-bit or fp32 state", i));
+            if (!t.m_absmax) return fail(Q8_ERR_NULL, at("m_absmax must be non-NULL", i));
+            if (!aligned(t.m_codes, 16) || !aligned(t.m_absmax, 4))
+                return fail(Q8_ERR_ALIGN, at("codes must be 16-byte and absmax 4-byte aligned", i));
+        } else {
+            if (!t.m32) return fail(Q8_ERR_NULL, at("state pointers (m_codes or m32) are NULL", i));
+            if (t.numel >= q8::kSmall) return fail(Q8_ERR_SIZE, at("fp32 state needs numel < 4096", i));
+            if (!aligned(t.m32, 16)) return fail(Q8_ERR_ALIGN, at("m32 must be 16-byte aligned", i));
+        }
+    }
+    if (ntensors == 0) return Q8_OK;
+    const q8::DevTables* tab = nullptr;
+    cudaError_t err = q8::device_tables(&tab);
+    if (err != cudaSuccess) return cuda_fail(err, "device set-up");
+
+    std::unique_ptr<q8::Step1Args> big(new q8::Step1Args());
+    std::unique_ptr<q8::Step1_32Args> small(new q8::Step1_32Args());
+    big->s = s;
+    big->tab = tab;
+    big->nt = 0;
+    big->blk_start[0] = 0;
+    small->s = s;
+    small->nt = 0;
+    auto flush_big = [&]() -> cudaError_t {
+        if (big->nt == 0) return cudaSuccess;
+        big->nblocks = big->blk_start[big->nt];
+        const cudaError_t e = q8::launch_step1(opt, *big, stream);
+        big->nt = 0;
+        big->blk_start[0] = 0;
+        return e;
+    };
+    auto flush_small = [&]() -> cudaError_t {
+        if (small->nt == 0) return cudaSuccess;
+        const cudaError_t e = q8::launch_step1_32(opt, *small, stream);
+        small->nt = 0;
+        return e;
+    };
+    running = 0;
+    for (int i = 0; i < ntensors; ++i) {
+        const q8_tensor8& t = list[i];
+        const uint64_t e0 = static_cast<uint64_t>(t.philox_offset >= 0 ? t.philox_offset : running);
+        running += t.numel;
+        if (t.numel == 0) continue;
+        if (t.m_codes) {
+            const int64_t nb = (t.numel + q8::kBlock - 1) / q8::kBlock;
+            if (big->nt == q8::kMaxList ||
+                static_cast<int64_t>(big->blk_start[big->nt]) + nb > std::numeric_limits<int32_t>::max()) {
+                if ((err = flush_big()) != cudaSuccess) return cuda_fail(err, "one-state step launch");
+            }
+            q8::Desc8& d = big->d[big->nt];
+            d.p = t.param;
+            d.g = t.grad;
+            d.mq = t.m_codes;
+            d.vq = nullptr;
+            d.ma = t.m_absmax;
+            d.va = nullptr;
+            d.n = t.numel;
+            d.e0 = e0;
+            big->blk_start[big->nt + 1] = big->blk_start[big->nt] + static_cast<int32_t>(nb);
+            ++big->nt;
+        } else {
+            if (small->nt == q8::kMaxList) {
+                if ((err = flush_small()) != cudaSuccess) return cuda_fail(err, "one-state step launch");
+            }
+            q8::Desc32& d = small->d[small->nt++];
+            d.p = t.param;
+            d.g = t.grad;
+            d.m = t.m32;
+            d.v = nullptr;
+            d.n = t.numel;
+            d.e0 = e0;
+        }
+    }
+    if ((err = flush_big()) != cudaSuccess) return cuda_fail(err, "one-state step launch");
+    if ((err = flush_small()) != cudaSuccess) return cuda_fail(err, "one-state step launch");
+    return Q8_OK;
+}
+
+void fill_common(q8::Scalars1& s, double lr, double wd, int64_t step, uint64_t seed, int32_t sr)
+{
+    s.lr_neg = static_cast<float>(-lr);
+    s.decay = static_cast<float>(1.0 - lr * wd);
+    s.wd = static_cast<float>(wd);
+    s.k0 = static_cast<uint32_t>(seed);
+    s.k1 = static_cast<uint32_t>(seed >> 32);
+    s.step = static_cast<uint32_t>(step);
+    s.sr = sr;
+}
+
 }  // namespace
 
 extern "C" {
 
-int q8_abi_version(void) { return 2; }
+int q8_abi_version(void) { return 3; }
 
 const char* q8_last_error(void) { return g_error.c_str(); }
 
@@ -308,6 +434,38 @@ int adamw_bf16_sr_step(const q8_tensor16* list, int ntensors, const q8_adamw_hpa
     }
     if ((err = flush()) != cudaSuccess) return cuda_fail(err, "adamw_bf16_sr_step launch");
     return Q8_OK;
+}
+
+int momentum8bit_sr_step(const q8_tensor8* list, int ntensors, const q8_momentum_hparams* hp,
+                         q8_stream_t stream)
+{
+    if (!hp) return fail(Q8_ERR_NULL, "hparams is NULL");
+    int rc = check_common(hp->lr, hp->weight_decay, hp->step, hp->sr);
+    if (rc != Q8_OK) return rc;
+    if ((rc = check_beta(hp->momentum, "momentum")) != Q8_OK) return rc;
+    q8::Scalars1 s{};
+    fill_common(s, hp->lr, hp->weight_decay, hp->step, hp->seed, hp->sr);
+    s.a = static_cast<float>(hp->momentum);
+    s.oma = static_cast<float>(1.0 - hp->momentum);
+    s.b = 0.0f;
+    s.omb = 0.0f;
+    return onestate_step(q8::kMomentum, list, ntensors, s, stream);
+}
+
+int lion8bit_sr_step(const q8_tensor8* list, int ntensors, const q8_lion_hparams* hp, q8_stream_t stream)
+{
+    if (!hp) return fail(Q8_ERR_NULL, "hparams is NULL");
+    int rc = check_common(hp->lr, hp->weight_decay, hp->step, hp->sr);
+    if (rc != Q8_OK) return rc;
+    if ((rc = check_beta(hp->beta1, "beta1")) != Q8_OK) return rc;
+    if ((rc = check_beta(hp->beta2, "beta2")) != Q8_OK) return rc;
+    q8::Scalars1 s{};
+    fill_common(s, hp->lr, hp->weight_decay, hp->step, hp->seed, hp->sr);
+    s.a = static_cast<float>(hp->beta1);
+    s.oma = static_cast<float>(1.0 - hp->beta1);
+    s.b = static_cast<float>(hp->beta2);
+    s.omb = static_cast<float>(1.0 - hp->beta2);
+    return onestate_step(q8::kLion, list, ntensors, s, stream);
 }
 
 }  // extern "C"

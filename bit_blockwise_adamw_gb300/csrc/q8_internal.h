@@ -111,7 +111,34 @@ struct Step16Args {
     Desc16 d[kMaxList];
 };
 
+// One-state optimizers (8-bit Momentum, 8-bit Lion): scalars rounded once to
+// float on the host; the tensor list reuses Desc8 / Desc32 with only the
+// first-moment fields set.
+enum { kMomentum = 0, kLion = 1 };
+
+struct Scalars1 {
+    float lr_neg, a, oma, b, omb, decay, wd;
+    uint32_t k0, k1, step;
+    int32_t sr;
+};
+
+struct Step1Args {
+    Scalars1 s;
+    const DevTables* tab;
+    int32_t nt;
+    int32_t nblocks;
+    int32_t blk_start[kMaxList + 1];
+    Desc8 d[kMaxList];
+};
+
+struct Step1_32Args {
+    Scalars1 s;
+    int32_t nt;
+    Desc32 d[kMaxList];
+};
+
 static_assert(sizeof(Step8Args) <= 32764, "kernel parameter space");
+static_assert(sizeof(Step1Args) <= 32764, "kernel parameter space");
 static_assert(sizeof(Step16Args) <= 32764, "kernel parameter space");
 static_assert(sizeof(Step32Args) <= 32764, "kernel parameter space");
 
@@ -125,6 +152,8 @@ int resident_ctas(const void* kernel, int threads, size_t smem);
 cudaError_t launch_step8(const Step8Args& a, cudaStream_t st);
 cudaError_t launch_step32(const Step32Args& a, cudaStream_t st);
 cudaError_t launch_step16(const Step16Args& a, cudaStream_t st);
+cudaError_t launch_step1(int opt, const Step1Args& a, cudaStream_t st);
+cudaError_t launch_step1_32(int opt, const Step1_32Args& a, cudaStream_t st);
 cudaError_t launch_quantize(const float* x, uint8_t* codes, float* absmax, int64_t n, int kind,
                             const DevTables* tab, cudaStream_t st);
 cudaError_t launch_dequantize(const uint8_t* codes, const float* absmax, float* x, int64_t n,

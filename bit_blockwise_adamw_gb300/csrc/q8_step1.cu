@@ -1,0 +1,301 @@
+// q8_step1.cu -- one-state optimizers with an 8-bit blockwise first moment
+// and the stochastically rounded BF16 parameter write: SGD with momentum
+// ("8-bit Optimizers via Block-wise Quantization", introduction: Adam and
+// Momentum states; PyTorch's SGD definition: dampening 0, weight decay added
+// to the gradient) and Lion ("Stochastic rounding support for 8-bit
+// optimizers", motivation: 8-bit Lion; Chen et al. 2023, decoupled decay).
+//
+// Same layout as the fused AdamW step: a persistent grid of 128-thread CTAs,
+// one 2048-element block per iteration, sixteen elements per thread, the
+// signed codebook and its cell table in shared memory, partial last blocks in
+// a tail kernel, tensors below 4096 elements on an fp32-state kernel.
+// Traffic: 8 bytes per parameter plus 8 per block (grad 2, param 2+2, code 1+1).
+#include "q8_device.cuh"
+
+namespace q8 {
+
+namespace {
+
+constexpr int kT1 = 128;
+constexpr int kV1 = 16;
+constexpr int kW1 = kT1 / 32;
+static_assert(kT1 * kV1 == kBlock, "one block per CTA iteration");
+
+struct Tables1 {               // the part of DevTables this kernel stages
+    float cs[256];
+    uint32_t cell_s[kCellSEntries];
+};
+static_assert(sizeof(Tables1) % 16 == 0, "staged 16 bytes at a time");
+constexpr int kSmem1 = static_cast<int>(sizeof(Tables1)) + 2 * kW1 * 4;
+
+__device__ __forceinline__ int find_tensor1(const int32_t* start, int nt, int gb)
+{
+    int lo = 0, hi = nt;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (start[mid] <= gb) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ const Tables1* stage1(const DevTables* tab, unsigned char* smem)
+{
+    Tables1* t = reinterpret_cast<Tables1*>(smem);
+    for (int i = threadIdx.x; i < 256; i += kT1) t->cs[i] = tab->cs[i];
+    const uint4* src = reinterpret_cast<const uint4*>(tab->cell_s);
+    uint4* dst = reinterpret_cast<uint4*>(t->cell_s);
+    for (int i = threadIdx.x; i < kCellSEntries / 4; i += kT1) dst[i] = src[i];
+    __syncthreads();
+    return t;
+}
+
+// The element update of a pair (fp32, each x*y + z fused).
+template <int OPT>
+__device__ __forceinline__ float2 onestate2(const Scalars1& s, float2 g, float2 p, float2& m)
+{
+    if constexpr (OPT == kMomentum) {
+        const float2 d = __ffma2_rn(splat(s.wd), p, g);
+        m = __ffma2_rn(splat(s.a), m, d);
+        return __ffma2_rn(splat(s.lr_neg), m, p);
+    } else {
+        const float2 c = __ffma2_rn(splat(s.a), m, __fmul2_rn(splat(s.oma), g));
+        const float2 u = make_float2(c.x > 0.0f ? 1.0f : (c.x < 0.0f ? -1.0f : 0.0f),
+                                     c.y > 0.0f ? 1.0f : (c.y < 0.0f ? -1.0f : 0.0f));
+        const float2 pn = __ffma2_rn(splat(s.lr_neg), u, __fmul2_rn(p, splat(s.decay)));
+        m = __ffma2_rn(splat(s.b), m, __fmul2_rn(splat(s.omb), g));
+        return pn;
+    }
+}
+
+template <int OPT>
+__device__ __forceinline__ float onestate(const Scalars1& s, float g, float p, float& m)
+{
+    if constexpr (OPT == kMomentum) {
+        const float d = __fmaf_rn(s.wd, p, g);
+        m = __fmaf_rn(s.a, m, d);
+        return __fmaf_rn(s.lr_neg, m, p);
+    } else {
+        const float c = __fmaf_rn(s.a, m, __fmul_rn(s.oma, g));
+        const float u = c > 0.0f ? 1.0f : (c < 0.0f ? -1.0f : 0.0f);
+        const float pn = __fmaf_rn(s.lr_neg, u, __fmul_rn(p, s.decay));
+        m = __fmaf_rn(s.b, m, __fmul_rn(s.omb, g));
+        return pn;
+    }
+}
+
+// One block; FULL = sixteen valid elements per thread.
+template <int OPT, bool SR, bool FULL>
+__device__ __forceinline__ void block1(const Scalars1& s, const Desc8& d, int lb, int it, const Tables1* tb,
+                                       uint32_t* red2)
+{
+    const int tid = threadIdx.x;
+    const int lane = tid & 31;
+    const int warp = tid >> 5;
+    const int64_t i0 = static_cast<int64_t>(lb) * kBlock + tid * kV1;
+    const int64_t rem = d.n - i0;
+    const float2 Mold = splat(d.ma[lb]);
+
+    uint32_t gw[8], pw[8], mc[4];
+    if constexpr (FULL) {
+        const uint4 g0 = ld_stream16(d.g + i0), g1 = ld_stream16(d.g + i0 + 8);
+        const uint4 p0 = ld_stream16(d.p + i0), p1 = ld_stream16(d.p + i0 + 8);
+        const uint4 mq = ld_stream16(d.mq + i0);
+        gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w; gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
+        pw[0] = p0.x; pw[1] = p0.y; pw[2] = p0.z; pw[3] = p0.w; pw[4] = p1.x; pw[5] = p1.y; pw[6] = p1.z; pw[7] = p1.w;
+        mc[0] = mq.x; mc[1] = mq.y; mc[2] = mq.z; mc[3] = mq.w;
+    } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) { gw[j] = 0; pw[j] = 0; }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) mc[j] = 0x7F7F7F7Fu;
+#pragma unroll
+        for (int j = 0; j < kV1; ++j) {
+            if (j < rem) {
+                gw[j >> 1] |= static_cast<uint32_t>(d.g[i0 + j]) << ((j & 1) * 16);
+                pw[j >> 1] |= static_cast<uint32_t>(d.p[i0 + j]) << ((j & 1) * 16);
+                const uint32_t bsh = (j & 3) * 8;
+                mc[j >> 2] = (mc[j >> 2] & ~(0xFFu << bsh)) | (static_cast<uint32_t>(d.mq[i0 + j]) << bsh);
+            }
+        }
+    }
+
+    float2 m[8];
+    uint32_t po[8];
+    uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    if constexpr (SR) {
+        const uint64_t E = d.e0 + static_cast<uint64_t>(i0);
+        Scalars ps{};
+        ps.k0 = s.k0; ps.k1 = s.k1; ps.step = s.step;
+        draws8(E, 0u, ps, r);
+        draws8(E + 8, 0u, ps, r + 4);
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const uint32_t cw = mc[k >> 1];
+        const int b0 = (k & 1) * 2;
+        m[k] = __fmul2_rn(make_float2(tb->cs[byte_of(cw, b0)], tb->cs[byte_of(cw, b0 + 1)]), Mold);
+        po[k] = round2<SR>(onestate2<OPT>(s, bf16x2(gw[k]), bf16x2(pw[k]), m[k]), r[k]);
+    }
+    if constexpr (FULL) {
+        st_stream16(d.p + i0, make_uint4(po[0], po[1], po[2], po[3]));
+        st_stream16(d.p + i0 + 8, make_uint4(po[4], po[5], po[6], po[7]));
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            if (2 * k >= rem) m[k].x = 0.0f;
+            if (2 * k + 1 >= rem) m[k].y = 0.0f;
+        }
+    }
+
+    float lm = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) lm = max3(lm, fabsf(m[k].x), fabsf(m[k].y));
+    const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(lm));
+    uint32_t* red = red2 + (it & 1) * kW1;
+    if (lane == 0) red[warp] = wm;
+    __syncthreads();
+    const float M = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, lane < kW1 ? red[lane] : 0u));
+
+    uint32_t mo[4];
+    if (M > 0.0f) {
+        const float im = __frcp_rn(M);
+#pragma unroll
+        for (int k = 0; k < 8; k += 2) {
+            mo[k >> 1] = pack4(code_signed_scaled(m[k].x, im, tb->cell_s), code_signed_scaled(m[k].y, im, tb->cell_s),
+                               code_signed_scaled(m[k + 1].x, im, tb->cell_s),
+                               code_signed_scaled(m[k + 1].y, im, tb->cell_s));
+        }
+    } else {
+        mo[0] = mo[1] = mo[2] = mo[3] = 0x7F7F7F7Fu;
+    }
+    if constexpr (FULL) {
+        st_stream16(d.mq + i0, make_uint4(mo[0], mo[1], mo[2], mo[3]));
+    } else {
+#pragma unroll
+        for (int j = 0; j < kV1; ++j) {
+            if (j < rem) {
+                d.p[i0 + j] = static_cast<uint16_t>(po[j >> 1] >> ((j & 1) * 16));
+                d.mq[i0 + j] = static_cast<uint8_t>(mo[j >> 2] >> ((j & 3) * 8));
+            }
+        }
+    }
+    if (tid == 0) d.ma[lb] = M;
+}
+
+__device__ __forceinline__ bool partial1(const Desc8& d, int lb)
+{
+    return static_cast<int64_t>(lb + 1) * kBlock > d.n;
+}
+
+template <int OPT, bool SR>
+__global__ void __launch_bounds__(kT1, 8) step1_kernel(const __grid_constant__ Step1Args a)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    const Tables1* tb = stage1(a.tab, smem);
+    uint32_t* red = reinterpret_cast<uint32_t*>(smem + sizeof(Tables1));
+    const int begin = static_cast<int>((static_cast<int64_t>(blockIdx.x) * a.nblocks) / gridDim.x);
+    const int end = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * a.nblocks) / gridDim.x);
+    int ti = begin < end ? find_tensor1(a.blk_start, a.nt, begin) : 0;
+    for (int gb = begin, it = 0; gb < end; ++gb) {
+        while (gb >= a.blk_start[ti + 1]) ++ti;
+        const Desc8& d = a.d[ti];
+        const int lb = gb - a.blk_start[ti];
+        if (partial1(d, lb)) continue;
+        block1<OPT, SR, true>(a.s, d, lb, it++, tb, red);
+    }
+}
+
+template <int OPT, bool SR>
+__global__ void __launch_bounds__(kT1) step1_tail_kernel(const __grid_constant__ Step1Args a)
+{
+    const Desc8& d = a.d[blockIdx.x];
+    const int lb = static_cast<int>((d.n - 1) / kBlock);
+    if (!partial1(d, lb)) return;
+    extern __shared__ __align__(16) unsigned char smem[];
+    const Tables1* tb = stage1(a.tab, smem);
+    uint32_t* red = reinterpret_cast<uint32_t*>(smem + sizeof(Tables1));
+    block1<OPT, SR, false>(a.s, d, lb, 0, tb, red);
+}
+
+// fp32-state path: one CTA per tensor (numel < 4096 = 512 threads x 8).
+constexpr int kSmall1 = kSmall / kVec;
+
+template <int OPT, bool SR>
+__global__ void __launch_bounds__(kSmall1) step1_32_kernel(const __grid_constant__ Step1_32Args a)
+{
+    const Desc32& d = a.d[blockIdx.x];
+    const Scalars1& s = a.s;
+    const int64_t i0 = static_cast<int64_t>(threadIdx.x) * kVec;
+    const int64_t rem = d.n - i0;
+    if (rem <= 0) return;
+    float pn[kVec];
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) {
+        if (j < rem) {
+            float m = d.m[i0 + j];
+            const float g = __uint_as_float(static_cast<uint32_t>(d.g[i0 + j]) << 16);
+            const float p = __uint_as_float(static_cast<uint32_t>(d.p[i0 + j]) << 16);
+            pn[j] = onestate<OPT>(s, g, p, m);
+            d.m[i0 + j] = m;
+        } else {
+            pn[j] = 0.0f;
+        }
+    }
+    uint32_t r[4] = {0, 0, 0, 0};
+    if constexpr (SR) {
+        Scalars ps{};
+        ps.k0 = s.k0; ps.k1 = s.k1; ps.step = s.step;
+        draws8(d.e0 + static_cast<uint64_t>(i0), 0u, ps, r);
+    }
+#pragma unroll
+    for (int j = 0; j < kVec; j += 2) {
+        const uint32_t w = round2<SR>(make_float2(pn[j], pn[j + 1]), r[j >> 1]);
+        if (j < rem) d.p[i0 + j] = static_cast<uint16_t>(w);
+        if (j + 1 < rem) d.p[i0 + j + 1] = static_cast<uint16_t>(w >> 16);
+    }
+}
+
+template <int OPT, bool SR>
+cudaError_t launch1(const Step1Args& a, bool has_partial, cudaStream_t st)
+{
+    static int full = 0;
+    if (full == 0) {
+        const void* k = reinterpret_cast<const void*>(step1_kernel<OPT, SR>);
+        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem1);
+        if (e != cudaSuccess) return e;
+        full = resident_ctas(k, kT1, kSmem1);
+        if (full <= 0) return cudaErrorUnknown;
+    }
+    const int grid = a.nblocks < full ? a.nblocks : full;
+    if (grid > 0) step1_kernel<OPT, SR><<<grid, kT1, kSmem1, st>>>(a);
+    if (has_partial && a.nt > 0) step1_tail_kernel<OPT, SR><<<a.nt, kT1, kSmem1, st>>>(a);
+    return cudaGetLastError();
+}
+
+template <int OPT>
+cudaError_t launch1_32(const Step1_32Args& a, cudaStream_t st)
+{
+    if (a.nt > 0) {
+        if (a.s.sr) step1_32_kernel<OPT, true><<<a.nt, kSmall1, 0, st>>>(a);
+        else step1_32_kernel<OPT, false><<<a.nt, kSmall1, 0, st>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_step1(int opt, const Step1Args& a, cudaStream_t st)
+{
+    bool has_partial = false;
+    for (int i = 0; i < a.nt; ++i) has_partial = has_partial || (a.d[i].n % kBlock) != 0;
+    if (opt == kMomentum)
+        return a.s.sr ? launch1<kMomentum, true>(a, has_partial, st) : launch1<kMomentum, false>(a, has_partial, st);
+    return a.s.sr ? launch1<kLion, true>(a, has_partial, st) : launch1<kLion, false>(a, has_partial, st);
+}
+
+cudaError_t launch_step1_32(int opt, const Step1_32Args& a, cudaStream_t st)
+{
+    return opt == kMomentum ? launch1_32<kMomentum>(a, st) : launch1_32<kLion>(a, st);
+}
+
+}  // namespace q8

@@ -179,6 +179,43 @@ int adamw_bf16_sr_step(const q8_tensor16* list, int ntensors, const q8_adamw_hpa
                        q8_stream_t stream);
 
 /*
+ * One-state optimizers with a signed 8-bit blockwise first moment and the
+ * same stochastically rounded BF16 parameter write ([BW] introduction: Adam
+ * and Momentum states; [SR] motivation: 8-bit Lion).  Each x*y + z is one
+ * fused fp32 multiply-add; scalars are rounded once to float.
+ *   SGD with momentum (PyTorch's definition: dampening 0, weight decay added
+ *   to the gradient): d = fma(wd, p, g); m = fma(momentum, m, d);
+ *   p = fma(-lr, m, p).
+ *   Lion (Chen et al. 2023, "Symbolic Discovery of Optimization Algorithms",
+ *   decoupled decay): c = fma(beta1, m, (1-beta1)*g); u = sign(c) (0 at 0);
+ *   p = fma(-lr, u, p*(1 - lr*wd)); m = fma(beta2, m, (1-beta2)*g).
+ * Hyper-parameters: lr, weight_decay >= 0 and finite; momentum, beta1, beta2
+ * in [0, 1); 1 <= step <= Q8_MAX_STEP (the Philox counter word); seed; sr.
+ * Tensor list: q8_tensor8 entries with m_codes + m_absmax (8-bit state; any
+ * length, block-aligned slices allowed) or m32 (fp32 state, numel < 4096);
+ * v_codes, v_absmax and v32 must be NULL.  The parameter draw of element E is
+ * r16(E) on Philox stream 0, as for adamw8bit_sr_step.
+ */
+typedef struct {
+    double lr, momentum, weight_decay;
+    int64_t step;
+    uint64_t seed;
+    int32_t sr;
+} q8_momentum_hparams;
+
+typedef struct {
+    double lr, beta1, beta2, weight_decay;
+    int64_t step;
+    uint64_t seed;
+    int32_t sr;
+} q8_lion_hparams;
+
+int momentum8bit_sr_step(const q8_tensor8* list, int ntensors, const q8_momentum_hparams* hp,
+                         q8_stream_t stream);
+int lion8bit_sr_step(const q8_tensor8* list, int ntensors, const q8_lion_hparams* hp,
+                     q8_stream_t stream);
+
+/*
  * The 16-bit random draws the steps use, for inspection: out[i] = r16(E) for
  * E = offset + i, where Philox4x32-10 (Salmon et al., SC'11) with key
  * (seed & 0xffffffff, seed >> 32) and counter (lo32(E/8), stream_id, step,
@@ -200,7 +237,7 @@ int q8_prepare_device(void);
 const char* q8_last_error(void);
 
 /* ABI version: bumped on any change of a signature or struct. */
-int q8_abi_version(void);   /* 2 */
+int q8_abi_version(void);   /* 3 */
 
 #ifdef __cplusplus
 }

@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version(lib):
-    assert q8.q8_abi_version() == 2
+    assert q8.q8_abi_version() == 3
 
 
 @pytest.mark.parametrize("kind", [q8.SIGNED, q8.UNSIGNED])
@@ -113,3 +113,21 @@ def test_codec_validation(lib):
     assert lib.q8_philox_fill(0, 1, 0, 0, 10, 0x1001, None) == -3
     assert lib.q8_codebook_init(0, None) == -1
     assert lib.q8_codebook_init(7, (C.c_float * 256)()) == -4
+
+
+def test_onestate_validation(lib):
+    def t1(**kw):
+        return _t8(v_codes=None, v_absmax=None, **kw)
+    good = B.MomentumHParams(1e-2, 0.9, 0.0, 1, 0, 1)
+    arr = (B._Tensor8 * 1)(_t8())                      # carries a second moment
+    assert lib.momentum8bit_sr_step(arr, 1, C.byref(good), None) == -4
+    arr = (B._Tensor8 * 1)(t1(m_absmax=None))
+    assert lib.momentum8bit_sr_step(arr, 1, C.byref(good), None) == -1
+    arr = (B._Tensor8 * 1)(t1(m_codes=0x3008))
+    assert lib.momentum8bit_sr_step(arr, 1, C.byref(good), None) == -3
+    for bad in (B.MomentumHParams(1e-2, 1.0, 0.0, 1, 0, 1), B.MomentumHParams(-1.0, 0.9, 0.0, 1, 0, 1),
+                B.MomentumHParams(1e-2, 0.9, 0.0, 0, 0, 1)):
+        assert lib.momentum8bit_sr_step(arr, 1, C.byref(bad), None) == -4
+    lion_bad = B.LionHParams(1e-4, 0.9, 1.5, 0.0, 1, 0, 1)
+    assert lib.lion8bit_sr_step((B._Tensor8 * 1)(t1()), 1, C.byref(lion_bad), None) == -4
+    assert lib.lion8bit_sr_step(None, 0, C.byref(B.LionHParams(1e-4, 0.9, 0.99, 0.0, 1, 0, 1)), None) == 0

@@ -1,0 +1,80 @@
+"""GPU parity of the 8-bit Momentum and 8-bit Lion steps (SR parameter write)
+against the oracle, bit for bit, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import bit_blockwise_adamw_gb300 as q8
+from bit_blockwise_adamw_gb300 import workloads as W
+import oracle as o
+
+from parity import u16
+
+pytestmark = pytest.mark.gpu
+
+OPTS = {"momentum": (o.MOMENTUM, q8.momentum8bit_sr_step), "lion": (o.LION, q8.lion8bit_sr_step)}
+
+
+def _hp(name, step, sr, wd=0.01):
+    if name == "momentum":
+        return (q8.momentum_hparams(lr=1e-2, momentum=0.9, weight_decay=wd, step=step, seed=3, sr=sr),
+                o.hparams(lr=1e-2, beta1=0.9, weight_decay=wd, step=step, seed=3, sr=sr))
+    return (q8.lion_hparams(lr=1e-4, beta1=0.9, beta2=0.99, weight_decay=wd, step=step, seed=3, sr=sr),
+            o.hparams(lr=1e-4, beta1=0.9, beta2=0.99, weight_decay=wd, step=step, seed=3, sr=sr))
+
+
+def _run(name, wl, device, steps, sr=1, offsets=None):
+    opt, fn = OPTS[name]
+    params = W.init_params(wl, device)
+    offsets = offsets or [-1] * len(params)
+    gpu = [q8.Tensor8.zeros_like(p, None, philox_offset=off, moments=1) for p, off in zip(params, offsets)]
+    host = [o.zeros_onestate(u16(p), np.zeros(p.numel(), np.uint16), philox_offset=off)
+            for p, off in zip(params, offsets)]
+    for step in range(1, steps + 1):
+        grads = W.make_grads(wl, step, device)
+        for a, b, g in zip(gpu, host, grads):
+            a.grad = g
+            b.grad = u16(g)
+        hg, hh = _hp(name, step, sr)
+        fn(gpu, hg)
+        o.onestate_sr_step(opt, host, hh)
+        torch.cuda.synchronize()
+        for i, (a, b) in enumerate(zip(gpu, host)):
+            where = "%s tensor %d step %d" % (name, i, step)
+            np.testing.assert_array_equal(u16(a.param), b.param, err_msg="param " + where)
+            if b.m_codes is not None:
+                np.testing.assert_array_equal(a.m_codes.cpu().numpy(), b.m_codes, err_msg="codes " + where)
+                np.testing.assert_array_equal(a.m_absmax.cpu().numpy().view(np.uint32),
+                                              b.m_absmax.view(np.uint32), err_msg="absmax " + where)
+            else:
+                np.testing.assert_array_equal(a.m32.cpu().numpy().view(np.uint32), b.m32.view(np.uint32),
+                                              err_msg="m32 " + where)
+
+
+@pytest.mark.parametrize("name", ["momentum", "lion"])
+@pytest.mark.parametrize("sr", [1, 0])
+def test_flat_full_parity(cuda_device, name, sr):
+    wl = W.custom("flat", [1 << 20], steps=6, outlier_rate=1e-3, outlier_factor=100.0, data_seed=90)
+    _run(name, wl, cuda_device, 6, sr=sr)
+
+
+@pytest.mark.parametrize("name", ["momentum", "lion"])
+def test_edge_sizes(cuda_device, name):
+    wl = W.custom("edges", [1, 7, 2047, 2048, 4095, 4096, 4097, 3 * 2048 + 1, 65536 + 24, 0, 300],
+                  steps=4, data_seed=91)
+    _run(name, wl, cuda_device, 4)
+
+
+@pytest.mark.parametrize("name", ["momentum", "lion"])
+def test_misaligned_offsets(cuda_device, name):
+    wl = W.custom("offs", [5000, 2048 * 3 + 5, 700], steps=3, data_seed=92)
+    _run(name, wl, cuda_device, 3, offsets=[3, (1 << 33) + 5, 11])
+
+
+@pytest.mark.parametrize("name", ["momentum", "lion"])
+def test_model_shaped_list(cuda_device, name):
+    """A GPT-2-shaped list of two layers (weights, biases, LayerNorm gains)."""
+    from bit_blockwise_adamw_gb300.workloads import _gpt2
+    wl = W.Workload("gpt2-2l", _gpt2(2, 256, 1024, vocab=1000, ctx=128), steps=3,
+                    hp={}, grad_std=1e-3, data_seed=93)
+    _run(name, wl, cuda_device, 3)
