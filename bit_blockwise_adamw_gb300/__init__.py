@@ -1,7 +1,8 @@
 """GB300 (sm_103a) fused 8-bit blockwise AdamW with stochastic rounding.
 
 The compute lives in libq8adamw.so (C ABI: include/q8adamw.h); this package
-is its Python binding plus a torch.optim front end.
+is its Python binding (same names as the C entry points) plus a torch.optim
+front end (bit_blockwise_adamw_gb300.optim).
 """
 from ._binding import (  # noqa: F401
     BLOCK, EXPORTS, MAX_STEP, SIGNED, SMALL_NUMEL, UNSIGNED, HParams, LionHParams, MomentumHParams,

@@ -1,0 +1,67 @@
+"""The torch.optim front end: the same bits as direct library calls, and a
+state_dict round trip that continues bit for bit."""
+import copy
+
+import pytest
+import torch
+
+import bit_blockwise_adamw_gb300 as q8
+from bit_blockwise_adamw_gb300 import optim
+
+pytestmark = pytest.mark.gpu
+
+
+def _params(dev, seed=0):
+    g = torch.Generator(device=dev).manual_seed(seed)
+    shapes = [(300, 64), (64,), (4096,), (1000, 7)]
+    return [torch.nn.Parameter((torch.randn(s, generator=g, device=dev) * 0.02).to(torch.bfloat16)) for s in shapes]
+
+
+def _grads(params, step, dev):
+    g = torch.Generator(device=dev).manual_seed(1000 + step)
+    for p in params:
+        p.grad = (torch.randn(p.shape, generator=g, device=dev) * 1e-3).to(torch.bfloat16)
+
+
+def test_adamw_front_end_equals_direct_calls(cuda_device):
+    a = _params(cuda_device)
+    b = [torch.nn.Parameter(p.detach().clone()) for p in a]
+    opt = optim.AdamW8bitSR(a, lr=1e-3, weight_decay=0.01, seed=5)
+    states = [q8.Tensor8.zeros_like(p.detach()) for p in b]
+    offs, run = [], 0
+    for p in b:
+        offs.append(run)
+        run += p.numel()
+    for step in range(1, 4):
+        _grads(a, step, cuda_device)
+        _grads(b, step, cuda_device)
+        opt.step()
+        for s, p, off in zip(states, b, offs):
+            s.param, s.grad, s.philox_offset = p.detach(), p.grad.detach(), off
+        q8.adamw8bit_sr_step(states, q8.hparams(lr=1e-3, weight_decay=0.01, step=step, seed=5))
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x.detach(), y.detach())
+
+
+@pytest.mark.parametrize("cls", [optim.AdamW8bitSR, optim.Momentum8bitSR, optim.Lion8bitSR, optim.AdamWBF16SR])
+def test_state_dict_resume(cuda_device, cls):
+    a = _params(cuda_device)
+    opt = cls(a, seed=7)
+    for step in range(1, 4):
+        _grads(a, step, cuda_device)
+        opt.step()
+    saved_params = [p.detach().clone() for p in a]
+    saved = copy.deepcopy(opt.state_dict())
+    for step in range(4, 7):
+        _grads(a, step, cuda_device)
+        opt.step()
+    b = [torch.nn.Parameter(p.clone()) for p in saved_params]
+    opt2 = cls(b, seed=7)
+    opt2.load_state_dict(saved)
+    for step in range(4, 7):
+        _grads(b, step, cuda_device)
+        opt2.step()
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x.detach(), y.detach())
