@@ -83,7 +83,7 @@ def algorithmic_bytes(wl, moments=2):
         if wl.state == "bf16":
             total += 14 * t.numel
         elif t.numel >= 4096:
-            total += (4 + 3 * moments) * t.numel + 8 * moments * ((t.numel + BLOCK - 1) // BLOCK)
+            total += (6 + 2 * moments) * t.numel + 8 * moments * ((t.numel + BLOCK - 1) // BLOCK)
         else:
             total += (6 + 8 * moments) * t.numel
     return total

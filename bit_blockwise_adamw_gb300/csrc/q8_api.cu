@@ -61,9 +61,7 @@ int make_scalars(const q8_adamw_hparams* hp, q8::Scalars* s)
     s->eps_t = static_cast<float>(hp->eps * root_bc2);
     s->step_size = static_cast<float>(hp->lr * root_bc2 / bc1);
     s->decay = static_cast<float>(1.0 - hp->lr * hp->weight_decay);
-    s->k0 = static_cast<uint32_t>(hp->seed);
-    s->k1 = static_cast<uint32_t>(hp->seed >> 32);
-    s->step = static_cast<uint32_t>(hp->step);
+    s->key = q8::philox_key(hp->seed, static_cast<uint32_t>(hp->step));
     s->sr = hp->sr;
     return Q8_OK;
 }
@@ -194,9 +192,7 @@ void fill_common(q8::Scalars1& s, double lr, double wd, int64_t step, uint64_t s
     s.lr_neg = static_cast<float>(-lr);
     s.decay = static_cast<float>(1.0 - lr * wd);
     s.wd = static_cast<float>(wd);
-    s.k0 = static_cast<uint32_t>(seed);
-    s.k1 = static_cast<uint32_t>(seed >> 32);
-    s.step = static_cast<uint32_t>(step);
+    s.key = q8::philox_key(seed, static_cast<uint32_t>(step));
     s.sr = sr;
 }
 
@@ -266,7 +262,7 @@ int q8_philox_fill(uint64_t seed, uint32_t step, uint32_t stream_id, uint64_t of
     if (n == 0) return Q8_OK;
     if (!out) return fail(Q8_ERR_NULL, "out is NULL");
     if (!aligned(out, 2)) return fail(Q8_ERR_ALIGN, "out must be 2-byte aligned");
-    const cudaError_t err = q8::launch_philox_fill(seed, step, stream_id, offset, n, out, stream);
+    const cudaError_t err = q8::launch_philox_fill(q8::philox_key(seed, step), stream_id, offset, n, out, stream);
     if (err != cudaSuccess) return cuda_fail(err, "q8_philox_fill launch");
     return Q8_OK;
 }

@@ -97,14 +97,10 @@ __global__ void __launch_bounds__(kThreads) dequantize_kernel(const uint8_t* __r
     }
 }
 
-__global__ void __launch_bounds__(kThreads) philox_fill_kernel(uint64_t seed, uint32_t step,
+__global__ void __launch_bounds__(kThreads) philox_fill_kernel(const __grid_constant__ PhiloxKey key,
                                                                uint32_t sid, uint64_t offset,
                                                                int64_t n, uint16_t* __restrict__ out)
 {
-    Scalars s{};
-    s.k0 = static_cast<uint32_t>(seed);
-    s.k1 = static_cast<uint32_t>(seed >> 32);
-    s.step = step;
     const uint64_t first = offset & ~uint64_t(7);
     const uint64_t last = offset + static_cast<uint64_t>(n);          // exclusive
     const uint64_t groups = (last - first + 7) / 8;
@@ -112,7 +108,7 @@ __global__ void __launch_bounds__(kThreads) philox_fill_kernel(uint64_t seed, ui
          g += static_cast<uint64_t>(gridDim.x) * kThreads) {
         const uint64_t E = first + 8 * g;
         uint32_t r[4];
-        draws8(E, sid, s, r);
+        draws8(E, sid, key, r);
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const uint64_t e = E + j;
@@ -154,8 +150,8 @@ cudaError_t launch_dequantize(const uint8_t* codes, const float* absmax, float* 
     return cudaGetLastError();
 }
 
-cudaError_t launch_philox_fill(uint64_t seed, uint32_t step, uint32_t stream_id, uint64_t offset,
-                               int64_t n, uint16_t* out, cudaStream_t st)
+cudaError_t launch_philox_fill(const PhiloxKey& key, uint32_t stream_id, uint64_t offset, int64_t n,
+                               uint16_t* out, cudaStream_t st)
 {
     if (n == 0) return cudaSuccess;
     static int full = 0;
@@ -163,8 +159,22 @@ cudaError_t launch_philox_fill(uint64_t seed, uint32_t step, uint32_t stream_id,
     const uint64_t groups = ((offset & 7) + static_cast<uint64_t>(n) + 7) / 8;
     const uint64_t want = (groups + kThreads - 1) / kThreads;
     const int grid = static_cast<int>(want < static_cast<uint64_t>(full) ? want : full);
-    philox_fill_kernel<<<grid, kThreads, 0, st>>>(seed, step, stream_id, offset, n, out);
+    philox_fill_kernel<<<grid, kThreads, 0, st>>>(key, stream_id, offset, n, out);
     return cudaGetLastError();
+}
+
+PhiloxKey philox_key(uint64_t seed, uint32_t step)
+{
+    PhiloxKey k{};
+    uint32_t k0 = static_cast<uint32_t>(seed), k1 = static_cast<uint32_t>(seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        k.kx[r] = k0;
+        k.ky[r] = k1;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+    k.step = step;
+    return k;
 }
 
 }  // namespace q8

@@ -16,10 +16,10 @@ __device__ __forceinline__ float2 bf16x2(uint32_t w) { return make_float2(bf16lo
 
 // ---------------------------------------------------------------- Philox
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of
-// (c0,c1,c2,c3) -> (hi(B*c2)^c1^k0, lo(B*c2), hi(A*c0)^c3^k1, lo(A*c0)) with
-// the key advanced by the Weyl increments between rounds.
+// (c0,c1,c2,c3) -> (hi(B*c2)^c1^k0, lo(B*c2), hi(A*c0)^c3^k1, lo(A*c0)), the
+// round keys taken from the host-formed schedule.
 __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3,
-                                               uint32_t k0, uint32_t k1)
+                                               const PhiloxKey& k)
 {
 #pragma unroll
     for (int round = 0; round < 10; ++round) {
@@ -27,12 +27,10 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
         const uint32_t hi0 = __umulhi(0xD2511F53u, c0);
         const uint32_t lo1 = 0xCD9E8D57u * c2;
         const uint32_t hi1 = __umulhi(0xCD9E8D57u, c2);
-        c0 = hi1 ^ c1 ^ k0;
+        c0 = hi1 ^ c1 ^ k.kx[round];
         c1 = lo1;
-        c2 = hi0 ^ c3 ^ k1;
+        c2 = hi0 ^ c3 ^ k.ky[round];
         c3 = lo0;
-        k0 += 0x9E3779B9u;
-        k1 += 0xBB67AE85u;
     }
     return make_uint4(c0, c1, c2, c3);
 }
@@ -43,19 +41,17 @@ __device__ __forceinline__ uint4 philox4x32_10(uint32_t c0, uint32_t c1, uint32_
 // elements E+2j (low half) and E+2j+1 (high half).  When E is not a multiple
 // of 8 the eight draws span two calls; the shift `E & 7` is uniform across a
 // tensor, so the branches below do not diverge inside a warp.
-__device__ __forceinline__ void draws8(uint64_t E, uint32_t sid, const Scalars& s, uint32_t r[4])
+__device__ __forceinline__ void draws8(uint64_t E, uint32_t sid, const PhiloxKey& k, uint32_t r[4])
 {
     const uint64_t grp = E >> 3;
     const uint32_t sh = static_cast<uint32_t>(E) & 7u;
-    const uint4 a = philox4x32_10(static_cast<uint32_t>(grp), sid, s.step,
-                                  static_cast<uint32_t>(grp >> 32), s.k0, s.k1);
+    const uint4 a = philox4x32_10(static_cast<uint32_t>(grp), sid, k.step, static_cast<uint32_t>(grp >> 32), k);
     if (sh == 0) {
         r[0] = a.x; r[1] = a.y; r[2] = a.z; r[3] = a.w;
         return;
     }
     const uint64_t g2 = grp + 1;
-    const uint4 b = philox4x32_10(static_cast<uint32_t>(g2), sid, s.step,
-                                  static_cast<uint32_t>(g2 >> 32), s.k0, s.k1);
+    const uint4 b = philox4x32_10(static_cast<uint32_t>(g2), sid, k.step, static_cast<uint32_t>(g2 >> 32), k);
     uint32_t w0 = a.x, w1 = a.y, w2 = a.z, w3 = a.w, w4 = b.x, w5 = b.y, w6 = b.z, w7 = b.w;
     if (sh & 4u) { w0 = w2; w1 = w3; w2 = w4; w3 = w5; w4 = w6; w5 = w7; }
     if (sh & 2u) { w0 = w1; w1 = w2; w2 = w3; w3 = w4; w4 = w5; }
@@ -124,12 +120,23 @@ __device__ __forceinline__ void moments2(const Scalars& s, float2 g, float2& m, 
     v = __ffma2_rn(splat(s.b2), v, __fmul2_rn(splat(s.omb2), __fmul2_rn(g, g)));
 }
 
+// m / (sqrt(v) + eps_t) of a pair, given sqrt(v).
+__device__ __forceinline__ float2 ratio2(const Scalars& s, float2 m, float2 root)
+{
+    const float2 den = __fadd2_rn(root, splat(s.eps_t));
+    return make_float2(__fdiv_rn(m.x, den.x), __fdiv_rn(m.y, den.y));
+}
+
+// p*decay - a_t*ratio of a pair.
+__device__ __forceinline__ float2 step2(const Scalars& s, float2 p, float2 ratio)
+{
+    return __ffma2_rn(splat(-s.step_size), ratio, __fmul2_rn(p, splat(s.decay)));
+}
+
 // The parameter update of a pair given sqrt(v): p*decay - a_t*(m/(sqrt(v)+eps_t)).
 __device__ __forceinline__ float2 param2(const Scalars& s, float2 p, float2 m, float2 root)
 {
-    const float2 ratio = make_float2(__fdiv_rn(m.x, __fadd_rn(root.x, s.eps_t)),
-                                     __fdiv_rn(m.y, __fadd_rn(root.y, s.eps_t)));
-    return __ffma2_rn(splat(-s.step_size), ratio, __fmul2_rn(p, splat(s.decay)));
+    return step2(s, p, ratio2(s, m, root));
 }
 
 __device__ __forceinline__ float2 adamw2(const Scalars& s, float2 g, float2 p, float2& m, float2& v)
@@ -170,11 +177,19 @@ __device__ __forceinline__ uint32_t sat_mul_bits(float x, float s)
 // y < 0 takes 127 - #{positive midpoints <= |y|}; the comparison key carries
 // 0xFF00 in its low half for y < 0 (above any base count, below the marker of
 // a cell without a midpoint), which turns "<" into "<=".
+__device__ __forceinline__ uint32_t signed_key(uint32_t a, uint32_t neg)
+{
+    // bytes (high to low): a.b1, a.b0, neg.b0, and the sign of a.b3 (0: a >= 0)
+    uint32_t k;
+    asm("prmt.b32 %0, %1, %2, 0x104B;" : "=r"(k) : "r"(a), "r"(neg));
+    return k;
+}
+
 __device__ __forceinline__ uint32_t code_signed_mag(uint32_t a, uint32_t neg, const uint32_t* cells)
 {
     const int cell = __viaddmax_s32(static_cast<int>(a >> kCellShift), kSignedCellBias, 0);
     const uint32_t e = cells[cell];
-    const uint32_t key = (a << 16) | (neg & 0xFF00u);
+    const uint32_t key = signed_key(a, neg);             // (a << 16) | (neg & 0xFF00)
     const uint32_t c = e + (key > e ? 1u : 0u);
     return 127u + ((c ^ neg) - neg);
 }

@@ -10,9 +10,10 @@
 namespace q8 {
 
 // Blocking ("8-bit Optimizers via Block-wise Quantization", method bullets:
-// 2048-element blocks).  A CTA of 256 threads owns one block per iteration,
-// eight contiguous elements per thread, so each thread makes one 16-byte load
-// of bf16 data, one 8-byte load of codes and one Philox call.
+// 2048-element blocks).  The codec, BF16-state and fp32-state kernels use
+// 256-thread CTAs with eight contiguous elements per thread (one 16-byte load
+// of bf16 data, one Philox call); the 8-bit step kernels use their own
+// 128-thread layout.
 constexpr int kBlock = 2048;
 constexpr int kThreads = 256;
 constexpr int kVec = 8;
@@ -48,10 +49,21 @@ struct alignas(16) DevTables {
 };
 static_assert(sizeof(DevTables) % 16 == 0, "tables are copied to shared memory 16 bytes at a time");
 
+// Philox4x32-10 key schedule of one call (Salmon, Moraes, Dror, Shaw, SC'11):
+// round r uses the key (k0 + r*0x9E3779B9, k1 + r*0xBB67AE85) mod 2^32, with
+// (k0, k1) = (low, high) 32 bits of the seed.  Formed once on the host, so
+// each round reads its key as a kernel-parameter operand.  `step` is counter
+// word 2.
+struct PhiloxKey {
+    uint32_t kx[10], ky[10];
+    uint32_t step;
+};
+PhiloxKey philox_key(uint64_t seed, uint32_t step);
+
 // Step scalars formed on the host in double and rounded once to float.
 struct Scalars {
     float b1, omb1, b2, omb2, eps_t, step_size, decay;
-    uint32_t k0, k1, step;
+    PhiloxKey key;
     int32_t sr;
 };
 
@@ -118,7 +130,7 @@ enum { kMomentum = 0, kLion = 1 };
 
 struct Scalars1 {
     float lr_neg, a, oma, b, omb, decay, wd;
-    uint32_t k0, k1, step;
+    PhiloxKey key;
     int32_t sr;
 };
 
@@ -158,7 +170,7 @@ cudaError_t launch_quantize(const float* x, uint8_t* codes, float* absmax, int64
                             const DevTables* tab, cudaStream_t st);
 cudaError_t launch_dequantize(const uint8_t* codes, const float* absmax, float* x, int64_t n,
                               int kind, const DevTables* tab, cudaStream_t st);
-cudaError_t launch_philox_fill(uint64_t seed, uint32_t step, uint32_t stream_id, uint64_t offset,
-                               int64_t n, uint16_t* out, cudaStream_t st);
+cudaError_t launch_philox_fill(const PhiloxKey& key, uint32_t stream_id, uint64_t offset, int64_t n,
+                               uint16_t* out, cudaStream_t st);
 
 }  // namespace q8

@@ -124,10 +124,8 @@ __device__ __forceinline__ void block1(const Scalars1& s, const Desc8& d, int lb
     uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if constexpr (SR) {
         const uint64_t E = d.e0 + static_cast<uint64_t>(i0);
-        Scalars ps{};
-        ps.k0 = s.k0; ps.k1 = s.k1; ps.step = s.step;
-        draws8(E, 0u, ps, r);
-        draws8(E + 8, 0u, ps, r + 4);
+        draws8(E, 0u, s.key, r);
+        draws8(E + 8, 0u, s.key, r + 4);
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -242,11 +240,7 @@ __global__ void __launch_bounds__(kSmall1) step1_32_kernel(const __grid_constant
         }
     }
     uint32_t r[4] = {0, 0, 0, 0};
-    if constexpr (SR) {
-        Scalars ps{};
-        ps.k0 = s.k0; ps.k1 = s.k1; ps.step = s.step;
-        draws8(d.e0 + static_cast<uint64_t>(i0), 0u, ps, r);
-    }
+    if constexpr (SR) draws8(d.e0 + static_cast<uint64_t>(i0), 0u, s.key, r);
 #pragma unroll
     for (int j = 0; j < kVec; j += 2) {
         const uint32_t w = round2<SR>(make_float2(pn[j], pn[j + 1]), r[j >> 1]);

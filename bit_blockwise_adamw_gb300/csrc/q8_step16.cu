@@ -69,9 +69,9 @@ __global__ void __launch_bounds__(kThreads, 4) step16_kernel(const __grid_consta
         const uint64_t E = d.e0 + static_cast<uint64_t>(i0);
         uint32_t rp[4] = {0, 0, 0, 0}, rm[4] = {0, 0, 0, 0}, rv[4] = {0, 0, 0, 0};
         if constexpr (SR) {
-            draws8(E, 0u, s, rp);
-            draws8(E, 1u, s, rm);
-            draws8(E, 2u, s, rv);
+            draws8(E, 0u, s.key, rp);
+            draws8(E, 1u, s.key, rm);
+            draws8(E, 2u, s.key, rv);
         }
         uint32_t po[4], mo[4], vo[4];
         float2 m[4], v[4];

@@ -165,8 +165,8 @@ __device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int
     uint32_t r[8] = {0, 0, 0, 0, 0, 0, 0, 0};
     if constexpr (SR) {
         const uint64_t E = d.e0 + static_cast<uint64_t>(i0);
-        draws8(E, 0u, s, r);
-        draws8(E + 8, 0u, s, r + 4);
+        draws8(E, 0u, s.key, r);
+        draws8(E + 8, 0u, s.key, r + 4);
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
@@ -328,7 +328,7 @@ __global__ void __launch_bounds__(kSmallThreads) step32_kernel(const __grid_cons
         }
     }
     uint32_t r[4] = {0, 0, 0, 0};
-    if constexpr (SR) draws8(d.e0 + static_cast<uint64_t>(i0), 0u, s, r);
+    if constexpr (SR) draws8(d.e0 + static_cast<uint64_t>(i0), 0u, s.key, r);
 #pragma unroll
     for (int j = 0; j < kVec; j += 2) {
         const uint32_t w = round2<SR>(make_float2(pn[j], pn[j + 1]), r[j >> 1]);
