@@ -154,17 +154,14 @@ __device__ __forceinline__ void block1(const Scalars1& s, const Desc8& d, int lb
     __syncthreads();
     const float M = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, lane < kW1 ? red[lane] : 0u));
 
+    // absmax 0 needs no branch: m * RN(1/0) saturates to +0, the zero code 127
     uint32_t mo[4];
-    if (M > 0.0f) {
-        const float im = __frcp_rn(M);
+    const float im = __frcp_rn(M);
 #pragma unroll
-        for (int k = 0; k < 8; k += 2) {
-            mo[k >> 1] = pack4(code_signed_scaled(m[k].x, im, tb->cell_s), code_signed_scaled(m[k].y, im, tb->cell_s),
-                               code_signed_scaled(m[k + 1].x, im, tb->cell_s),
-                               code_signed_scaled(m[k + 1].y, im, tb->cell_s));
-        }
-    } else {
-        mo[0] = mo[1] = mo[2] = mo[3] = 0x7F7F7F7Fu;
+    for (int k = 0; k < 8; k += 2) {
+        mo[k >> 1] = pack4(code_signed_scaled(m[k].x, im, tb->cell_s), code_signed_scaled(m[k].y, im, tb->cell_s),
+                           code_signed_scaled(m[k + 1].x, im, tb->cell_s),
+                           code_signed_scaled(m[k + 1].y, im, tb->cell_s));
     }
     if constexpr (FULL) {
         st_stream16(d.mq + i0, make_uint4(mo[0], mo[1], mo[2], mo[3]));

@@ -23,7 +23,7 @@ def _hp(name, step, sr, wd=0.01):
             o.hparams(lr=1e-4, beta1=0.9, beta2=0.99, weight_decay=wd, step=step, seed=3, sr=sr))
 
 
-def _run(name, wl, device, steps, sr=1, offsets=None):
+def _run(name, wl, device, steps, sr=1, offsets=None, grad_hook=None, wd=0.01):
     opt, fn = OPTS[name]
     params = W.init_params(wl, device)
     offsets = offsets or [-1] * len(params)
@@ -32,10 +32,12 @@ def _run(name, wl, device, steps, sr=1, offsets=None):
             for p, off in zip(params, offsets)]
     for step in range(1, steps + 1):
         grads = W.make_grads(wl, step, device)
+        if grad_hook:
+            grad_hook(step, grads)
         for a, b, g in zip(gpu, host, grads):
             a.grad = g
             b.grad = u16(g)
-        hg, hh = _hp(name, step, sr)
+        hg, hh = _hp(name, step, sr, wd)
         fn(gpu, hg)
         o.onestate_sr_step(opt, host, hh)
         torch.cuda.synchronize()
@@ -63,6 +65,19 @@ def test_edge_sizes(cuda_device, name):
     wl = W.custom("edges", [1, 7, 2047, 2048, 4095, 4096, 4097, 3 * 2048 + 1, 65536 + 24, 0, 300],
                   steps=4, data_seed=91)
     _run(name, wl, cuda_device, 4)
+
+
+@pytest.mark.parametrize("name", ["momentum", "lion"])
+def test_zero_gradient_blocks(cuda_device, name):
+    """Blocks with an all-zero first moment (absmax 0, zero code 127); no
+    weight decay, which momentum would otherwise add to the gradient."""
+    wl = W.custom("zeros", [4 * 2048, 2048 * 3 + 100, 5000], steps=4, data_seed=94)
+
+    def hook(step, grads):
+        grads[0][2048:4096].zero_()
+        grads[1][3 * 2048:].zero_()
+        grads[2].zero_()
+    _run(name, wl, cuda_device, 4, grad_hook=hook, wd=0.0)
 
 
 @pytest.mark.parametrize("name", ["momentum", "lion"])

@@ -28,14 +28,17 @@ def pool():
     p.join()
 
 
-def _run_full(wl, device, steps=None, sr=1, offsets=None, split=None):
-    """Run `wl` on both sides for `steps`, comparing everything after each step."""
+def _run_full(wl, device, steps=None, sr=1, offsets=None, split=None, grad_hook=None):
+    """Run `wl` on both sides for `steps`, comparing everything after each step
+    (`grad_hook(step, grads)` may edit the step's gradients in place first)."""
     steps = steps or wl.steps
     params = W.init_params(wl, device)
     gpu = gpu_states8(params, offsets)
     host = host_states8([u16(p) for p in params], offsets)
     for step in range(1, steps + 1):
         grads = W.make_grads(wl, step, device)
+        if grad_hook:
+            grad_hook(step, grads)
         for g_gpu, g_host, gr in zip(gpu, host, grads):
             g_gpu.grad = gr
             g_host.grad = u16(gr)
@@ -66,6 +69,22 @@ def test_edge_sizes_mixed_paths(cuda_device, sr):
     tensor in one list, 4 steps, both rounding modes."""
     wl = W.custom("edges", EDGE_SIZES, steps=4, outlier_rate=0.01, outlier_factor=50.0, data_seed=77)
     _run_full(wl, cuda_device, sr=sr)
+
+
+def test_zero_gradient_blocks(cuda_device):
+    """Blocks whose moments are all zero (absmax 0, zero codes 127 and 0):
+    zero gradients from the first step in some blocks, a whole tensor and a
+    partial last block, and zero gradients again after nonzero steps, where the
+    moments decay but stay nonzero."""
+    wl = W.custom("zeros", [4 * 2048, 2048 * 3 + 100, 5000, 4096], steps=5, data_seed=79)
+
+    def hook(step, grads):
+        grads[0][2048:4096].zero_()                     # one full block, every step
+        grads[1][3 * 2048:].zero_()                     # the partial last block
+        grads[2].zero_()                                # a whole tensor
+        if step >= 3:
+            grads[3].zero_()                            # zero after nonzero steps
+    _run_full(wl, cuda_device, grad_hook=hook)
 
 
 def test_explicit_misaligned_offsets(cuda_device):
