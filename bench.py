@@ -31,6 +31,7 @@ import torch  # noqa: E402
 METRIC = "fused AdamW8bit+SR step: Gparams/s and HBM GB/s (% of peak), 1 GB300"
 UNIT = "Gparams/s"
 BLOCK = 2048
+NOMINAL_HBM_GBS = 7900.0          # NVIDIA's HBM3e figure for GB300, for context only
 
 
 def parse():
@@ -173,9 +174,9 @@ def traffic_per_launch(kernel, units):
 
 # ---------------------------------------------------------------- CPU oracle
 
-def oracle_sample_time(wl, nblocks, seed=0):
-    """Time the oracle (single-threaded C) on a seeded sample of the
-    workload's 2048-blocks for one step; returns (params, seconds)."""
+def _oracle_sample(wl, nblocks, seed):
+    """A seeded sample of the workload's 2048-blocks as oracle states, and a
+    function that runs one step of the oracle over them; returns (params, run)."""
     import oracle as o
     from bit_blockwise_adamw_gb300 import workloads as W
     rng = np.random.default_rng(seed)
@@ -195,17 +196,52 @@ def oracle_sample_time(wl, nblocks, seed=0):
     if wl.state == "bf16":
         states = [o.State16(p[k].copy(), g[k].copy(), np.zeros(BLOCK, np.uint16), np.zeros(BLOCK, np.uint16))
                   for k in range(nblocks)]
+        one = o.adamw_bf16_tensor
     else:
         states = [o.State8.zeros(p[k].copy(), g[k].copy(), eight_bit=True) for k in range(nblocks)]
+        one = o.adamw8bit_tensor
     e0 = [offs[bigs[pick[k]]] for k in range(nblocks)]
+
+    def run():
+        for k, st in enumerate(states):
+            one(st, e0[k], hp)
+    return nblocks * BLOCK, run
+
+
+def oracle_sample_time(wl, nblocks, seed=0):
+    """Time the oracle (single-threaded C) on a seeded sample of the
+    workload's 2048-blocks for one step; returns (params, seconds)."""
+    n, run = _oracle_sample(wl, nblocks, seed)
     t0 = time.perf_counter()
-    for k, s in enumerate(states):
-        if wl.state == "bf16":
-            o.adamw_bf16_tensor(s, e0[k], hp)
-        else:
-            o.adamw8bit_tensor(s, e0[k], hp)
-    dt = time.perf_counter() - t0
-    return nblocks * BLOCK, dt
+    run()
+    return n, time.perf_counter() - t0
+
+
+def _oracle_proc(wl, nblocks, seed, barrier, results):
+    """One process of the block-parallel timing: build its own seeded share of
+    the sample, wait for the others, then time its oracle calls."""
+    n, run = _oracle_sample(wl, nblocks, seed)
+    barrier.wait()
+    t0 = time.perf_counter()
+    run()
+    results.put((n, t0, time.perf_counter()))
+
+
+def oracle_parallel_time(wl, nblocks_per_proc, procs):
+    """The same oracle, block-parallel: `procs` spawned processes (blocks are
+    independent), each with its own seeded sample, started together.
+    Returns (params, wall seconds from the first start to the last end)."""
+    import multiprocessing as mp
+    ctx = mp.get_context("spawn")
+    barrier, results = ctx.Barrier(procs), ctx.Queue()
+    ps = [ctx.Process(target=_oracle_proc, args=(wl, nblocks_per_proc, 100 + i, barrier, results))
+          for i in range(procs)]
+    for q in ps:
+        q.start()
+    got = [results.get(timeout=600) for _ in ps]
+    for q in ps:
+        q.join()
+    return sum(r[0] for r in got), max(r[2] for r in got) - min(r[1] for r in got)
 
 
 def run_reference(args):
@@ -254,14 +290,18 @@ def main():
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
 
-    from bit_blockwise_adamw_gb300 import build as B
-    B.build()
-    import bit_blockwise_adamw_gb300 as q8
-    from bit_blockwise_adamw_gb300 import workloads as W
-
     def barrier():
         if world > 1:
             torch.distributed.barrier()
+
+    # one rank per node compiles (a no-op when the library is current); the
+    # others wait for it instead of racing on the same build directory
+    from bit_blockwise_adamw_gb300 import build as B
+    if local == 0:
+        B.build()
+    barrier()
+    import bit_blockwise_adamw_gb300 as q8
+    from bit_blockwise_adamw_gb300 import workloads as W
 
     wl = workload(args)
     q8.q8_prepare_device()
@@ -333,6 +373,7 @@ def main():
     traffic = traffic_per_launch(kernel, numel / nl) if nl == 1 else None
     roofline = {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                 "frac": achieved / peak, "traffic": traffic, "kernel": kernel,
+                "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
                 "algorithmic_bytes_per_launch": abytes / nl, "peak_source": peak_kind,
                 "median_ms_per_step": statistics.median(per), "min_ms_per_step": min(per)}
 
@@ -341,7 +382,7 @@ def main():
     e2e = None
     if not args.no_e2e and args.optimizer == "adamw":
         e2e = run_e2e(args, wl, states, step_fn, hp, t, device, world, barrier)
-        t += args.e2e_steps + 1
+        t += args.e2e_steps + 3
 
     cpu = None
     if not args.no_cpu_baseline and rank == 0 and args.optimizer == "adamw":
@@ -349,6 +390,14 @@ def main():
         cpu = {"value": n / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
                "sample": "%d seeded 2048-blocks (%d params) of %s, one step, single-threaded C oracle"
                          % (args.cpu_blocks, n, wl.name)}
+        procs = len(os.sched_getaffinity(0))
+        if procs > 1:
+            per = max(1, args.cpu_blocks // 4)
+            n, dt = oracle_parallel_time(wl, per, procs)
+            cpu["block_parallel"] = {
+                "value": n / dt / 1e9, "unit": UNIT, "cores": procs, "kind": "oracle",
+                "sample": "%d processes x %d seeded 2048-blocks (%d params) of %s, one step each, started together"
+                          % (procs, per, n, wl.name)}
 
     if rank == 0:
         line = {
@@ -373,8 +422,13 @@ def run_e2e(args, wl, states, step_fn, hp, t, device, world, barrier):
     """Per step: H2D copy of this step's grads from pinned host memory, the
     step through the C ABI, D2H copy of the updated params into pinned host
     memory.  The list is cut into chunks (explicit Philox offsets keep the
-    bits identical to one call) so the copies of one chunk overlap the step of
-    another on three streams."""
+    bits identical to one call) so the copies of one chunk overlap the step
+    of another.  Two copy schedules: "duplex" (H2D and D2H on their own
+    streams, running at once) and "serial" (both in order on one copy stream,
+    one chunk's grads ahead of the compute stream).  Which is faster depends
+    on the host link: concurrent H2D + D2H reached 343 GB/s on one GB300 machine
+    and 99 GB/s on another, against about 200 GB/s one direction at a time.
+    One untimed step of each picks the schedule for the timed steps."""
     import bit_blockwise_adamw_gb300 as q8
     from bit_blockwise_adamw_gb300 import workloads as W
     offs = W.philox_offsets(wl)
@@ -388,44 +442,84 @@ def run_e2e(args, wl, states, step_fn, hp, t, device, world, barrier):
     for hg, s in zip(host_g, states):
         hg.copy_(s.grad)
     packs = [(q8.pack_tensor16 if wl.state == "bf16" else q8.pack_tensor8)([states[i] for i in c]) for c in chunks]
-    s_in, s_cmp, s_out = (torch.cuda.Stream(device) for _ in range(3))
+    s_in, s_out, s_cmp = (torch.cuda.Stream(device) for _ in range(3))
 
-    def one_step(tt):
-        for c, pk in zip(chunks, packs):
-            e_in = torch.cuda.Event()
-            with torch.cuda.stream(s_in):
-                for i in c:
-                    states[i].grad.copy_(host_g[i], non_blocking=True)
-                e_in.record(s_in)
+    def record(stream):
+        e = torch.cuda.Event()
+        e.record(stream)
+        return e
+
+    def grads_in(c, stream):
+        with torch.cuda.stream(stream):
+            for i in chunks[c]:
+                states[i].grad.copy_(host_g[i], non_blocking=True)
+        return record(stream)
+
+    def params_out(c, stream):
+        with torch.cuda.stream(stream):
+            for i in chunks[c]:
+                host_p[i].copy_(states[i].param, non_blocking=True)
+
+    def step_serial(tt):
+        e_in = grads_in(0, s_in)
+        for c, pk in enumerate(packs):
             s_cmp.wait_event(e_in)
             step_fn(pk, hp(tt), s_cmp)
-            e_c = torch.cuda.Event()
-            e_c.record(s_cmp)
-            s_out.wait_event(e_c)
-            with torch.cuda.stream(s_out):
-                for i in c:
-                    host_p[i].copy_(states[i].param, non_blocking=True)
+            e_c = record(s_cmp)
+            if c + 1 < len(packs):
+                e_in = grads_in(c + 1, s_in)
+            s_in.wait_event(e_c)
+            params_out(c, s_in)
 
-    one_step(t + 1)                      # warm-up
-    torch.cuda.synchronize(device)
-    barrier()
-    t0 = time.perf_counter()
-    for k in range(args.e2e_steps):
-        one_step(t + 2 + k)
-    torch.cuda.synchronize(device)
-    barrier()
-    dt = time.perf_counter() - t0
+    done_cmp = [None] * len(packs)              # per chunk, from the previous step
+    done_out = [None] * len(packs)
+
+    def step_duplex(tt):
+        for c, pk in enumerate(packs):
+            if done_cmp[c] is not None:
+                s_in.wait_event(done_cmp[c])    # the last step has read these grads
+            e_in = grads_in(c, s_in)
+            s_cmp.wait_event(e_in)
+            if done_out[c] is not None:
+                s_cmp.wait_event(done_out[c])   # the last step's params are out
+            step_fn(pk, hp(tt), s_cmp)
+            done_cmp[c] = record(s_cmp)
+            s_out.wait_event(done_cmp[c])
+            params_out(c, s_out)
+            done_out[c] = record(s_out)
+
+    def timed(fn, first, k):
+        torch.cuda.synchronize(device)
+        barrier()
+        t0 = time.perf_counter()
+        for j in range(k):
+            fn(first + j)
+        torch.cuda.synchronize(device)
+        barrier()
+        return time.perf_counter() - t0
+
+    tt = t + 1
+    timed(step_duplex, tt, 1)                  # warm-up
+    d_duplex = timed(step_duplex, tt + 1, 1)
+    d_serial = timed(step_serial, tt + 2, 1)
     if world > 1:
-        tt = torch.tensor([dt], device=device)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        dt = float(tt.item())
+        tt2 = torch.tensor([d_duplex, d_serial], device=device)
+        torch.distributed.all_reduce(tt2, op=torch.distributed.ReduceOp.MAX)
+        d_duplex, d_serial = (float(x) for x in tt2.tolist())
+    mode, fn = ("duplex", step_duplex) if d_duplex <= d_serial else ("serial", step_serial)
+    dt = timed(fn, tt + 3, args.e2e_steps)
+    if world > 1:
+        tt3 = torch.tensor([dt], device=device)
+        torch.distributed.all_reduce(tt3, op=torch.distributed.ReduceOp.MAX)
+        dt = float(tt3.item())
     nb = 2 * wl.numel
     for s in states:
         s.philox_offset = -1
     return {"value": world * wl.numel * args.e2e_steps / dt / 1e9, "unit": UNIT,
             "h2d_bytes_per_step": nb, "d2h_bytes_per_step": nb, "steps": args.e2e_steps,
-            "ms_per_step": 1e3 * dt / args.e2e_steps,
-            "note": "pinned host grads in, params out, %d chunks on 3 streams" % len(chunks)}
+            "ms_per_step": 1e3 * dt / args.e2e_steps, "schedule": mode,
+            "trial_ms": {"duplex": 1e3 * d_duplex, "serial": 1e3 * d_serial},
+            "note": "pinned host grads in, params out, %d chunks, %s copy schedule" % (len(chunks), mode)}
 
 
 if __name__ == "__main__":

@@ -225,33 +225,6 @@ __device__ __forceinline__ uint32_t pack4(uint32_t q0, uint32_t q1, uint32_t q2,
 // Byte j (0..3) of w, zero-extended.
 __device__ __forceinline__ uint32_t byte_of(uint32_t w, int j) { return __byte_perm(w, 0u, 0x4440 | j); }
 
-// ---------------------------------------------------------------- L2 prefetch
-// Ask the L2 to fetch [p, p + bytes) from DRAM now (a hint: it completes
-// asynchronously and is never waited for).  bytes must be a multiple of 16.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
-// Prefetch the inputs of local block `lb` of an 8-bit-state tensor into L2:
-// grad, param, the m codes and (if the tensor has them) the v codes, clipped
-// to whole 16-byte chunks inside the tensor.
-__device__ __forceinline__ void prefetch_block(const Desc8& d, int lb)
-{
-    const int64_t first = static_cast<int64_t>(lb) * kBlock;
-    const int64_t n = d.n - first < kBlock ? d.n - first : kBlock;
-    const uint32_t b16 = static_cast<uint32_t>(n * 2) & ~15u;
-    const uint32_t b8 = static_cast<uint32_t>(n) & ~15u;
-    if (b16) {
-        prefetch_l2(d.g + first, b16);
-        prefetch_l2(d.p + first, b16);
-    }
-    if (b8) {
-        prefetch_l2(d.mq + first, b8);
-        if (d.vq) prefetch_l2(d.vq + first, b8);
-    }
-}
-
 // ---------------------------------------------------------------- misc
 __device__ __forceinline__ float max3(float a, float b, float c)
 {
