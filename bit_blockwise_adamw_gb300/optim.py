@@ -8,21 +8,65 @@ parameter is given a fixed global Philox offset when it is first seen (the
 running element count in group order), so the stochastic-rounding draws of
 an element depend only on (seed, step, element) and a restored optimizer
 continues bit for bit.
+
+The descriptor table a step passes to the library is built once per group
+(state pointers do not move); each step only refreshes its param and grad
+pointers.
 """
+import numpy as np
 import torch
 
 from . import _binding as B
 
+_T8_FIELDS = [f[0] for f in B._Tensor8._fields_]
+_T16_FIELDS = [f[0] for f in B._Tensor16._fields_]
+
+
+def _ptr(t):
+    return 0 if t is None else t.data_ptr()
+
+
+def _check_param(p):
+    if p.dtype != torch.bfloat16 or not p.is_cuda or not p.is_contiguous():
+        raise ValueError("parameters must be contiguous bf16 CUDA tensors")
+    g = p.grad
+    if g.dtype != torch.bfloat16 or not g.is_contiguous() or g.shape != p.shape or g.device != p.device:
+        raise ValueError("gradients must be contiguous bf16 tensors shaped like their parameters")
+    return g
+
+
+class _Table:
+    """A group's packed descriptors: an int64 table whose rows have the
+    layout of the library's tensor struct (all fields 8 bytes), viewed as a
+    ctypes array without a copy."""
+
+    def __init__(self, params, rows, struct, fields):
+        self.params = list(params)
+        self.np = np.array([[row[f] for f in fields] for row in rows], dtype=np.int64).reshape(len(rows),
+                                                                                            len(fields))
+        self.c = (struct * len(rows)).from_buffer(self.np)
+
+    def matches(self, params):
+        return len(params) == len(self.params) and all(a is b for a, b in zip(params, self.params))
+
+    def refresh(self):
+        for i, p in enumerate(self.params):
+            g = _check_param(p)
+            self.np[i, 0] = p.data_ptr()
+            self.np[i, 1] = g.data_ptr()
+        return self.c
+
 
 class _FrontEnd(torch.optim.Optimizer):
-    """Philox offset bookkeeping and a state_dict round trip that keeps each
-    state tensor's dtype (torch.optim casts floating-point state to the
-    parameter's dtype on load, which would turn uint8 codes and float32
-    absmax into bf16)."""
+    """Philox offset bookkeeping, the cached descriptor tables and a
+    state_dict round trip that keeps each state tensor's dtype (torch.optim
+    casts floating-point state to the parameter's dtype on load, which would
+    turn uint8 codes and float32 absmax into bf16)."""
 
     def __init__(self, params, defaults):
         super().__init__(params, defaults)
         self._next_offset = 0
+        self._tables = {}
 
     def _offset(self, p, state):
         if "philox_offset" not in state:
@@ -41,24 +85,14 @@ class _FrontEnd(torch.optim.Optimizer):
                     self.state[p][k] = v.to(device=p.device).clone()
         used = [int(s["philox_offset"]) + p.numel() for p, s in self.state.items() if "philox_offset" in s]
         self._next_offset = max(used, default=0)
+        self._tables = {}
 
-
-class _Q8Optimizer(_FrontEnd):
-    moments = 2
-
-    def _tensor8(self, p):
-        if p.dtype != torch.bfloat16 or not p.is_cuda or not p.is_contiguous():
-            raise ValueError("parameters must be contiguous bf16 CUDA tensors")
-        state = self.state[p]
-        off = self._offset(p, state)
-        if "m_codes" not in state and "m32" not in state:
-            t = B.Tensor8.zeros_like(p.detach(), moments=self.moments)
-            for k in ("m_codes", "v_codes", "m_absmax", "v_absmax", "m32", "v32"):
-                if getattr(t, k) is not None:
-                    state[k] = getattr(t, k)
-        return B.Tensor8(p.detach(), p.grad.detach(), state.get("m_codes"), state.get("v_codes"),
-                         state.get("m_absmax"), state.get("v_absmax"), state.get("m32"), state.get("v32"),
-                         philox_offset=off)
+    def _table(self, gi, params):
+        t = self._tables.get(gi)
+        if t is None or not t.matches(params):
+            t = _Table(params, [self._row(p) for p in params], *self._struct)
+            self._tables[gi] = t
+        return t.refresh()
 
     @torch.no_grad()
     def step(self, closure=None):
@@ -66,13 +100,32 @@ class _Q8Optimizer(_FrontEnd):
         if closure is not None:
             with torch.enable_grad():
                 loss = closure()
-        for group in self.param_groups:
-            tensors = [self._tensor8(p) for p in group["params"] if p.grad is not None]
-            if not tensors:
+        for gi, group in enumerate(self.param_groups):
+            params = [p for p in group["params"] if p.grad is not None]
+            if not params:
                 continue
+            arr = self._table(gi, params)
             group["step"] = group.get("step", 0) + 1
-            self._run(group, tensors)
+            self._run(group, arr)
         return loss
+
+
+class _Q8Optimizer(_FrontEnd):
+    moments = 2
+    _struct = (B._Tensor8, _T8_FIELDS)
+
+    def _row(self, p):
+        _check_param(p)
+        state = self.state[p]
+        off = self._offset(p, state)
+        if "m_codes" not in state and "m32" not in state:
+            t = B.Tensor8.zeros_like(p.detach(), moments=self.moments)
+            for k in ("m_codes", "v_codes", "m_absmax", "v_absmax", "m32", "v32"):
+                if getattr(t, k) is not None:
+                    state[k] = getattr(t, k)
+        row = {k: _ptr(state.get(k)) for k in ("m_codes", "v_codes", "m_absmax", "v_absmax", "m32", "v32")}
+        row.update(param=p.data_ptr(), grad=p.grad.data_ptr(), numel=p.numel(), philox_offset=off)
+        return row
 
 
 class AdamW8bitSR(_Q8Optimizer):
@@ -84,11 +137,11 @@ class AdamW8bitSR(_Q8Optimizer):
         super().__init__(params, dict(lr=lr, betas=betas, eps=eps, weight_decay=weight_decay, seed=seed,
                                       sr=int(stochastic_rounding)))
 
-    def _run(self, group, tensors):
+    def _run(self, group, arr):
         b1, b2 = group["betas"]
-        B.adamw8bit_sr_step(tensors, B.hparams(lr=group["lr"], beta1=b1, beta2=b2, eps=group["eps"],
-                                               weight_decay=group["weight_decay"], step=group["step"],
-                                               seed=group["seed"], sr=group["sr"]))
+        B.adamw8bit_sr_step(arr, B.hparams(lr=group["lr"], beta1=b1, beta2=b2, eps=group["eps"],
+                                           weight_decay=group["weight_decay"], step=group["step"],
+                                           seed=group["seed"], sr=group["sr"]))
 
 
 class Momentum8bitSR(_Q8Optimizer):
@@ -99,10 +152,10 @@ class Momentum8bitSR(_Q8Optimizer):
         super().__init__(params, dict(lr=lr, momentum=momentum, weight_decay=weight_decay, seed=seed,
                                       sr=int(stochastic_rounding)))
 
-    def _run(self, group, tensors):
-        B.momentum8bit_sr_step(tensors, B.momentum_hparams(lr=group["lr"], momentum=group["momentum"],
-                                                           weight_decay=group["weight_decay"],
-                                                           step=group["step"], seed=group["seed"], sr=group["sr"]))
+    def _run(self, group, arr):
+        B.momentum8bit_sr_step(arr, B.momentum_hparams(lr=group["lr"], momentum=group["momentum"],
+                                                       weight_decay=group["weight_decay"],
+                                                       step=group["step"], seed=group["seed"], sr=group["sr"]))
 
 
 class Lion8bitSR(_Q8Optimizer):
@@ -113,44 +166,35 @@ class Lion8bitSR(_Q8Optimizer):
         super().__init__(params, dict(lr=lr, betas=betas, weight_decay=weight_decay, seed=seed,
                                       sr=int(stochastic_rounding)))
 
-    def _run(self, group, tensors):
+    def _run(self, group, arr):
         b1, b2 = group["betas"]
-        B.lion8bit_sr_step(tensors, B.lion_hparams(lr=group["lr"], beta1=b1, beta2=b2,
-                                                   weight_decay=group["weight_decay"], step=group["step"],
-                                                   seed=group["seed"], sr=group["sr"]))
+        B.lion8bit_sr_step(arr, B.lion_hparams(lr=group["lr"], beta1=b1, beta2=b2,
+                                               weight_decay=group["weight_decay"], step=group["step"],
+                                               seed=group["seed"], sr=group["sr"]))
 
 
 class AdamWBF16SR(_FrontEnd):
     """BF16-state AdamW with stochastic rounding of params and both moments
     (adamw_bf16_sr_step)."""
+    _struct = (B._Tensor16, _T16_FIELDS)
 
     def __init__(self, params, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=1e-2, seed=0,
                  stochastic_rounding=True):
         super().__init__(params, dict(lr=lr, betas=betas, eps=eps, weight_decay=weight_decay, seed=seed,
                                       sr=int(stochastic_rounding)))
 
-    @torch.no_grad()
-    def step(self, closure=None):
-        loss = None
-        if closure is not None:
-            with torch.enable_grad():
-                loss = closure()
-        for group in self.param_groups:
-            tensors = []
-            for p in group["params"]:
-                if p.grad is None:
-                    continue
-                st = self.state[p]
-                off = self._offset(p, st)
-                if "m" not in st:
-                    st["m"] = torch.zeros_like(p)
-                    st["v"] = torch.zeros_like(p)
-                tensors.append(B.Tensor16(p.detach(), p.grad.detach(), st["m"], st["v"], off))
-            if not tensors:
-                continue
-            group["step"] = group.get("step", 0) + 1
-            b1, b2 = group["betas"]
-            B.adamw_bf16_sr_step(tensors, B.hparams(lr=group["lr"], beta1=b1, beta2=b2, eps=group["eps"],
-                                                    weight_decay=group["weight_decay"], step=group["step"],
-                                                    seed=group["seed"], sr=group["sr"]))
-        return loss
+    def _row(self, p):
+        _check_param(p)
+        st = self.state[p]
+        off = self._offset(p, st)
+        if "m" not in st:
+            st["m"] = torch.zeros_like(p)
+            st["v"] = torch.zeros_like(p)
+        return dict(param=p.data_ptr(), grad=p.grad.data_ptr(), m=st["m"].data_ptr(), v=st["v"].data_ptr(),
+                    numel=p.numel(), philox_offset=off)
+
+    def _run(self, group, arr):
+        b1, b2 = group["betas"]
+        B.adamw_bf16_sr_step(arr, B.hparams(lr=group["lr"], beta1=b1, beta2=b2, eps=group["eps"],
+                                            weight_decay=group["weight_decay"], step=group["step"],
+                                            seed=group["seed"], sr=group["sr"]))
