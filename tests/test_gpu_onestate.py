@@ -93,3 +93,32 @@ def test_model_shaped_list(cuda_device, name):
     wl = W.Workload("gpt2-2l", _gpt2(2, 256, 1024, vocab=1000, ctx=128), steps=3,
                     hp={}, grad_std=1e-3, data_seed=93)
     _run(name, wl, cuda_device, 3)
+
+
+@pytest.mark.parametrize("name", ["momentum", "lion"])
+def test_sharded_step_equals_unsharded(cuda_device, name):
+    """Three data-parallel ranks emulated in sequence on one GPU, each updating
+    only its block-aligned slices with global Philox offsets: the same bits as
+    the unsharded one-state step."""
+    from bit_blockwise_adamw_gb300 import sharding
+    _, fn = OPTS[name]
+    wl = W.custom("shard1", [2048 * 20 + 7, 300, 4096, 2048 * 9, 65536 + 24], steps=3, data_seed=95)
+    params = W.init_params(wl, cuda_device)
+    whole = [q8.Tensor8.zeros_like(p.clone(), None, moments=1) for p in params]
+    split = [q8.Tensor8.zeros_like(p.clone(), None, moments=1) for p in params]
+    for step in range(1, 4):
+        grads = W.make_grads(wl, step, cuda_device)
+        for a, b, g in zip(whole, split, grads):
+            a.grad = g
+            b.grad = g
+        hg, _ = _hp(name, step, 1)
+        fn(whole, hg)
+        for rank in range(3):
+            fn(sharding.shard(split, 3, rank), hg)
+    torch.cuda.synchronize()
+    for a, b in zip(whole, split):
+        assert torch.equal(a.param, b.param)
+        if a.m_codes is not None:
+            assert torch.equal(a.m_codes, b.m_codes) and torch.equal(a.m_absmax, b.m_absmax)
+        else:
+            assert torch.equal(a.m32, b.m32)

@@ -65,3 +65,29 @@ def test_state_dict_resume(cuda_device, cls):
     torch.cuda.synchronize()
     for x, y in zip(a, b):
         assert torch.equal(x.detach(), y.detach())
+
+
+def test_param_groups_and_missing_grads(cuda_device):
+    """Two groups with their own lr, one parameter without a gradient in one
+    step: each group equals direct calls with its own hyper-parameters and a
+    parameter without a gradient is left alone (its Philox offset stays
+    reserved)."""
+    a = _params(cuda_device)
+    b = [torch.nn.Parameter(p.detach().clone()) for p in a]
+    opt = optim.AdamW8bitSR([{"params": a[:2], "lr": 1e-3}, {"params": a[2:], "lr": 3e-4}], seed=2)
+    states = [q8.Tensor8.zeros_like(p.detach()) for p in b]
+    offs = [0, a[0].numel(), a[0].numel() + a[1].numel(), a[0].numel() + a[1].numel() + a[2].numel()]
+    for step in range(1, 3):
+        _grads(a, step, cuda_device)
+        _grads(b, step, cuda_device)
+        if step == 2:
+            a[3].grad = None
+        opt.step()
+        for s, p, off in zip(states, b, offs):
+            s.param, s.grad, s.philox_offset = p.detach(), p.grad.detach(), off
+        q8.adamw8bit_sr_step(states[:2], q8.hparams(lr=1e-3, weight_decay=0.01, step=step, seed=2))
+        q8.adamw8bit_sr_step(states[2:] if step == 1 else states[2:3],
+                             q8.hparams(lr=3e-4, weight_decay=0.01, step=step, seed=2))
+    torch.cuda.synchronize()
+    for x, y in zip(a, b):
+        assert torch.equal(x.detach(), y.detach())
