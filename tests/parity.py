@@ -97,11 +97,11 @@ class SampledRun:
     """Run a full-size workload on the GPU while recording the inputs of the
     sampled blocks (and of every small tensor) for an oracle replay."""
 
-    def __init__(self, wl, device, fraction, steps=None):
+    def __init__(self, wl, device, fraction, steps=None, extra_blocks=()):
         self.wl = wl
         self.steps = steps or wl.steps
         self.device = device
-        self.picks = W.sample_blocks(wl, fraction)
+        self.picks = sorted(set(W.sample_blocks(wl, fraction)) | set(extra_blocks))
         self.small = wl.small_tensors() if wl.state == "8bit" else []
         self.offsets = W.philox_offsets(wl)
         self.by_tensor = {}

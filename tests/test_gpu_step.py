@@ -204,6 +204,20 @@ def test_full_size_sampled_parity(cuda_device, pool, name, fraction):
     assert compared > 0
 
 
+@pytest.mark.parametrize("state", ["8bit", "bf16"])
+def test_tensor_beyond_2_31_elements(cuda_device, pool, state):
+    """One tensor of 2^31 + 6221 elements (more elements than a signed 32-bit
+    index reaches, with a partial last block) after a small one: the blocks on
+    both sides of element 2^31, the first and the last, and a seeded sample,
+    replayed by the oracle over two steps."""
+    n = (1 << 31) + 3 * 2048 + 77
+    wl = W.custom("huge-" + state, [5000, n], steps=2, data_seed=85, state=state)
+    edge = (1 << 31) // 2048
+    run = SampledRun(wl, cuda_device, 2e-6, extra_blocks=[(1, edge - 1), (1, edge), (1, edge + 1)])
+    run.run()
+    assert run.check(pool) > 0
+
+
 @pytest.mark.parametrize("world", [2, 3, 8])
 def test_sharded_step_equals_unsharded(cuda_device, world):
     """N data-parallel ranks emulated in sequence on one GPU: each updates only
