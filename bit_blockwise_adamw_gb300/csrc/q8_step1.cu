@@ -49,6 +49,14 @@ __device__ __forceinline__ const Tables1* stage1(const DevTables* tab, unsigned 
     return t;
 }
 
+// sign(c) as a float: +-1 with the sign bit of c, and +0 for +-0 and NaN
+// (|c| > 0 is false for both), built from the bits: one compare, one logic
+// op and one select instead of two compares and two selects.
+__device__ __forceinline__ float sign1(float c)
+{
+    return fabsf(c) > 0.0f ? __uint_as_float((__float_as_uint(c) & 0x80000000u) | 0x3F800000u) : 0.0f;
+}
+
 // The element update of a pair (fp32, each x*y + z fused).
 template <int OPT>
 __device__ __forceinline__ float2 onestate2(const Scalars1& s, float2 g, float2 p, float2& m)
@@ -59,8 +67,7 @@ __device__ __forceinline__ float2 onestate2(const Scalars1& s, float2 g, float2 
         return __ffma2_rn(splat(s.lr_neg), m, p);
     } else {
         const float2 c = __ffma2_rn(splat(s.a), m, __fmul2_rn(splat(s.oma), g));
-        const float2 u = make_float2(c.x > 0.0f ? 1.0f : (c.x < 0.0f ? -1.0f : 0.0f),
-                                     c.y > 0.0f ? 1.0f : (c.y < 0.0f ? -1.0f : 0.0f));
+        const float2 u = make_float2(sign1(c.x), sign1(c.y));
         const float2 pn = __ffma2_rn(splat(s.lr_neg), u, __fmul2_rn(p, splat(s.decay)));
         m = __ffma2_rn(splat(s.b), m, __fmul2_rn(splat(s.omb), g));
         return pn;
@@ -76,7 +83,7 @@ __device__ __forceinline__ float onestate(const Scalars1& s, float g, float p, f
         return __fmaf_rn(s.lr_neg, m, p);
     } else {
         const float c = __fmaf_rn(s.a, m, __fmul_rn(s.oma, g));
-        const float u = c > 0.0f ? 1.0f : (c < 0.0f ? -1.0f : 0.0f);
+        const float u = sign1(c);
         const float pn = __fmaf_rn(s.lr_neg, u, __fmul_rn(p, s.decay));
         m = __fmaf_rn(s.b, m, __fmul_rn(s.omb, g));
         return pn;
