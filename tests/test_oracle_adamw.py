@@ -241,3 +241,61 @@ def test_multiply_adds_are_fused():
         unfused = np.float32(np.float32(p * np.float32(s.decay)) - np.float32(np.float32(s.step_size) * ratio))
         fused_differs += int(unfused != pn)
     assert fused_differs > 0          # the cases do tell the two readings apart
+
+
+def test_eight_bit_step_is_the_composition_of_its_pinned_parts():
+    """At a later step (nonzero 8-bit state, partial last block), the 8-bit
+    tensor step equals, element by element: dequantize the codes ([BW] method
+    bullets: lookup table times block absmax), the fp32 AdamW element update,
+    blockwise requantization of the new m and v, and the stochastically
+    rounded parameter write with the element's own Philox draw -- each part
+    pinned separately in this directory."""
+    rng = np.random.default_rng(21)
+    n = 2 * 2048 + 333
+    p = (np.asarray(rng.standard_normal(n) * 0.02, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    g = (np.asarray(rng.standard_normal(n) * 1e-3, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    m0 = (rng.standard_normal(n) * 1e-4).astype(np.float32)
+    v0 = (rng.random(n) * 1e-8).astype(np.float32)
+    mc, ma = o.quantize(o.SIGNED, m0)
+    vc, va = o.quantize(o.UNSIGNED, v0)
+    hp = o.hparams(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=7, seed=13)
+    E0 = 12345
+    st = o.State8(p.copy(), g, mc.copy(), vc.copy(), ma.copy(), va.copy())
+    o.adamw8bit_tensor(st, E0, hp)
+
+    s = o.step_scalars(hp)
+    m = o.dequantize(o.SIGNED, mc, ma)
+    v = o.dequantize(o.UNSIGNED, vc, va)
+    pf = np.zeros(n, np.float32)
+    for i in range(n):
+        pf[i], m[i], v[i] = o.adamw_element(s, o.bf16_to_f32(g[i]), o.bf16_to_f32(p[i]), m[i], v[i])
+    want_mc, want_ma = o.quantize(o.SIGNED, m)
+    want_vc, want_va = o.quantize(o.UNSIGNED, v)
+    want_p = np.array([o.sr_bf16(pf[i], o.r16(13, 7, 0, E0 + i)) for i in range(n)], np.uint16)
+    assert np.array_equal(st.param, want_p)
+    assert np.array_equal(st.m_codes, want_mc) and np.array_equal(st.v_codes, want_vc)
+    assert np.array_equal(st.m_absmax.view(np.uint32), want_ma.view(np.uint32))
+    assert np.array_equal(st.v_absmax.view(np.uint32), want_va.view(np.uint32))
+
+
+def test_bf16_step_is_the_composition_of_its_pinned_parts():
+    """BF16 state at a later step: every element equals the fp32 element
+    update followed by stochastic rounding of p, m and v with the draws of
+    Philox streams 0, 1 and 2 at that element ("Stochastic rounding of AdamW
+    momentums": fp32 maths, stochastically rounded write-back)."""
+    rng = np.random.default_rng(22)
+    n = 3000
+    p, g = _tensor(rng, n)
+    m0 = _bf16(rng.standard_normal(n) * 1e-4)
+    v0 = _bf16(np.abs(rng.standard_normal(n)) * 1e-8)
+    hp = o.hparams(lr=1.2e-3, weight_decay=0.1, step=9, seed=31)
+    E0 = 777
+    st = o.State16(p.copy(), g, m0.copy(), v0.copy(), philox_offset=E0)
+    o.adamw_bf16_sr_step([st], hp)
+    s = o.step_scalars(hp)
+    for i in range(n):
+        pn, mn, vn = o.adamw_element(s, o.bf16_to_f32(g[i]), o.bf16_to_f32(p[i]), o.bf16_to_f32(m0[i]),
+                                     o.bf16_to_f32(v0[i]))
+        assert st.param[i] == o.sr_bf16(pn, o.r16(31, 9, 0, E0 + i))
+        assert st.m[i] == o.sr_bf16(mn, o.r16(31, 9, 1, E0 + i))
+        assert st.v[i] == o.sr_bf16(vn, o.r16(31, 9, 2, E0 + i))

@@ -126,3 +126,29 @@ def test_list_routing_and_offsets(opt):
         o.onestate_sr_step(opt, [st], hp)
     for a, b in zip(whole, parts):
         assert np.array_equal(a.param, b.param)
+
+
+@pytest.mark.parametrize("opt", [MOM, LION])
+def test_eight_bit_step_is_the_composition_of_its_pinned_parts(opt):
+    """At a later step (nonzero 8-bit state, partial last block): dequantize,
+    the element update, blockwise requantization of the new m and the
+    stochastically rounded parameter write with the element's stream-0 draw."""
+    rng = np.random.default_rng(23)
+    n = 2 * 2048 + 555
+    p = _bf16(rng.standard_normal(n) * 0.02)
+    g = _bf16(rng.standard_normal(n) * 1e-3)
+    mc, ma = o.quantize(o.SIGNED, (rng.standard_normal(n) * 1e-3).astype(np.float32))
+    hp = o.hparams(lr=1e-3, beta1=0.9, beta2=0.99, weight_decay=0.01, step=5, seed=17)
+    E0 = 4242
+    st = o.State8(p.copy(), g, m_codes=mc.copy(), m_absmax=ma.copy())
+    o.onestate8bit_tensor(opt, st, E0, hp)
+    s = o.step_scalars1(opt, hp)
+    m = o.dequantize(o.SIGNED, mc, ma)
+    pf = np.zeros(n, np.float32)
+    for i in range(n):
+        pf[i], m[i] = o.onestate_element(opt, s, o.bf16_to_f32(g[i]), o.bf16_to_f32(p[i]), m[i])
+    want_mc, want_ma = o.quantize(o.SIGNED, m)
+    want_p = np.array([o.sr_bf16(pf[i], o.r16(17, 5, 0, E0 + i)) for i in range(n)], np.uint16)
+    assert np.array_equal(st.param, want_p)
+    assert np.array_equal(st.m_codes, want_mc)
+    assert np.array_equal(st.m_absmax.view(np.uint32), want_ma.view(np.uint32))
