@@ -9,4 +9,4 @@ from ._binding import (  # noqa: F401
     Q8Error, Tensor8, Tensor16, adamw8bit_sr_step, adamw_bf16_sr_step, hparams, library_path,
     lion8bit_sr_step, lion_hparams, load_library, momentum8bit_sr_step, momentum_hparams,
     pack_tensor8, pack_tensor16, q8_abi_version, q8_blockwise_dequantize, q8_blockwise_quantize,
-    q8_codebook_init, q8_last_error, q8_philox_fill, q8_prepare_device)
+    q8_codebook_init, q8_last_error, q8_philox_fill, q8_prepare_device, q8_selftest_sqrt_div)

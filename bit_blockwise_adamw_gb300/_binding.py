@@ -26,7 +26,7 @@ _STATUS = {-1: "Q8_ERR_NULL", -2: "Q8_ERR_SIZE", -3: "Q8_ERR_ALIGN", -4: "Q8_ERR
 # every symbol the header declares
 EXPORTS = ("q8_codebook_init", "q8_blockwise_quantize", "q8_blockwise_dequantize",
            "adamw8bit_sr_step", "adamw_bf16_sr_step", "momentum8bit_sr_step", "lion8bit_sr_step",
-           "q8_philox_fill", "q8_prepare_device", "q8_last_error", "q8_abi_version")
+           "q8_philox_fill", "q8_selftest_sqrt_div", "q8_prepare_device", "q8_last_error", "q8_abi_version")
 
 
 class Q8Error(RuntimeError):
@@ -93,6 +93,7 @@ def load_library(path: Optional[str] = None):
     L.momentum8bit_sr_step.argtypes = [C.POINTER(_Tensor8), C.c_int, C.POINTER(MomentumHParams), S]
     L.lion8bit_sr_step.argtypes = [C.POINTER(_Tensor8), C.c_int, C.POINTER(LionHParams), S]
     L.q8_philox_fill.argtypes = [C.c_uint64, C.c_uint32, C.c_uint32, C.c_uint64, C.c_int64, P, S]
+    L.q8_selftest_sqrt_div.argtypes = [P, S]
     L.q8_prepare_device.argtypes = []
     L.q8_last_error.argtypes = []
     L.q8_last_error.restype = C.c_char_p
@@ -180,6 +181,14 @@ def q8_philox_fill(seed: int, step: int, stream_id: int, offset: int, out: torch
     assert out.element_size() == 2, "out holds 16-bit draws (int16 or uint16)"
     _check("q8_philox_fill", load_library().q8_philox_fill(
         seed, step, stream_id, offset, out.numel(), _ptr(out), _stream(stream)))
+
+
+def q8_selftest_sqrt_div(counts: torch.Tensor, stream=None) -> None:
+    """Device self-test of the packed square root and division; counts:
+    int64[6] on the GPU (reciprocal mismatches, d values checked, quotient
+    mismatches, pairs checked, square-root mismatches, v values checked)."""
+    assert counts.dtype == torch.int64 and counts.numel() >= 6 and counts.is_contiguous()
+    _check("q8_selftest_sqrt_div", load_library().q8_selftest_sqrt_div(_ptr(counts), _stream(stream)))
 
 
 @dataclass

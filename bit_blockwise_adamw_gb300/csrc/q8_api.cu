@@ -63,6 +63,7 @@ int make_scalars(const q8_adamw_hparams* hp, q8::Scalars* s)
     s->decay = static_cast<float>(1.0 - hp->lr * hp->weight_decay);
     s->key = q8::philox_key(hp->seed, static_cast<uint32_t>(hp->step));
     s->sr = hp->sr;
+    s->fast_div = (s->eps_t >= 0x1p-100f && s->eps_t <= 0x1p20f) ? 1 : 0;
     return Q8_OK;
 }
 
@@ -200,7 +201,7 @@ void fill_common(q8::Scalars1& s, double lr, double wd, int64_t step, uint64_t s
 
 extern "C" {
 
-int q8_abi_version(void) { return 3; }
+int q8_abi_version(void) { return 4; }
 
 const char* q8_last_error(void) { return g_error.c_str(); }
 
@@ -251,6 +252,15 @@ int q8_blockwise_dequantize(const uint8_t* codes, const float* absmax, float* x,
     if (err != cudaSuccess) return cuda_fail(err, "device set-up");
     err = q8::launch_dequantize(codes, absmax, x, n, kind, tab, stream);
     if (err != cudaSuccess) return cuda_fail(err, "q8_blockwise_dequantize launch");
+    return Q8_OK;
+}
+
+int q8_selftest_sqrt_div(uint64_t* counts, q8_stream_t stream)
+{
+    if (!counts) return fail(Q8_ERR_NULL, "counts is NULL");
+    if (!aligned(counts, 8)) return fail(Q8_ERR_ALIGN, "counts must be 8-byte aligned");
+    const cudaError_t err = q8::launch_selftest_sqrt_div(counts, stream);
+    if (err != cudaSuccess) return cuda_fail(err, "q8_selftest_sqrt_div launch");
     return Q8_OK;
 }
 

@@ -109,8 +109,8 @@ __device__ __forceinline__ uint32_t round2(float2 x, uint32_t r)
 //   p = fma(-a_t, m / (sqrt(v) + eps_t), p*decay)
 // Pairs use the packed fp32x2 instructions (per lane identical to the scalar
 // _rn operations).  Every product feeds an explicit fma or nothing, so the
-// compiler has no multiply-add left to contract; the square root, the eps add
-// and the division stay scalar.
+// compiler has no multiply-add left to contract; the square root stays
+// scalar, the division is packed where it is provably exact (below).
 __device__ __forceinline__ float2 splat(float x) { return make_float2(x, x); }
 
 // The moment updates of a pair: m = fma(b1, m, (1-b1)*g), v = fma(b2, v, (1-b2)*g*g).
@@ -118,6 +118,49 @@ __device__ __forceinline__ void moments2(const Scalars& s, float2 g, float2& m, 
 {
     m = __ffma2_rn(splat(s.b1), m, __fmul2_rn(splat(s.omb1), g));
     v = __ffma2_rn(splat(s.b2), v, __fmul2_rn(splat(s.omb2), __fmul2_rn(g, g)));
+}
+
+// ---------------------------------------------------------------- division
+// Correctly rounded quotients on the packed fp32x2 unit.  y = RN(1/d) comes
+// from the hardware's approximate reciprocal and one Newton-Raphson step,
+// y = y0 + y0*(1 - d*y0) with each multiply-add fused; this equals the IEEE
+// reciprocal for every normal d whose reciprocal is normal (checked over all
+// of them, q8_selftest_sqrt_div).  Then Markstein's correction ("Computation
+// of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): q0 = RN(m*y), r = RN(m - d*q0) (one fma),
+// q = RN(q0 + r*y) (one fma) is RN(m/d) when y = RN(1/d) and no intermediate
+// leaves the normal range.  Callers use it only inside kDivSafe* bounds and
+// fall back to the IEEE division otherwise.
+constexpr float kDivMinM = 0x1p-90f;      // |m| at least this (and nonzero: the sign of 0)
+constexpr float kDivMaxM = 0x1p26f;       // |m| at most this
+constexpr float kDivMaxV = 0x1p40f;       // v at most this, so sqrt(v) <= 2^20
+// with eps_t in [2^-100, 2^20] (host flag Scalars::fast_div): d in [2^-100, 2^21],
+// 1/d normal, |q| in [2^-111, 2^126], the remainder's scale |m|*2^-23 normal.
+
+__device__ __forceinline__ float rcp_approx(float d)
+{
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(d));
+    return y;
+}
+
+__device__ __forceinline__ float2 neg2(float2 x) { return make_float2(-x.x, -x.y); }
+
+// RN(1/d) of a pair (d normal with a normal reciprocal).
+__device__ __forceinline__ float2 recip2(float2 d)
+{
+    const float2 y0 = make_float2(rcp_approx(d.x), rcp_approx(d.y));
+    const float2 e = __ffma2_rn(neg2(d), y0, make_float2(1.0f, 1.0f));
+    return __ffma2_rn(y0, e, y0);
+}
+
+// RN(m/d) of a pair inside the bounds above.
+__device__ __forceinline__ float2 div2_rn(float2 m, float2 d)
+{
+    const float2 y = recip2(d);
+    const float2 q0 = __fmul2_rn(m, y);
+    const float2 r = __ffma2_rn(neg2(d), q0, m);
+    return __ffma2_rn(r, y, q0);
 }
 
 // m / (sqrt(v) + eps_t) of a pair, given sqrt(v).
@@ -131,6 +174,35 @@ __device__ __forceinline__ float2 ratio2(const Scalars& s, float2 m, float2 root
 __device__ __forceinline__ float2 step2(const Scalars& s, float2 p, float2 ratio)
 {
     return __ffma2_rn(splat(-s.step_size), ratio, __fmul2_rn(p, splat(s.decay)));
+}
+
+// RN(sqrt(v)) of a pair: the hardware's approximate reciprocal square root
+// y and one Newton-Raphson (Heron) correction, s = s0 + (v - s0*s0)*(y/2)
+// with s0 = RN(v*y), each multiply-add fused.  Equal to the IEEE square root
+// for every normal v >= 2^-102 (checked over all of them,
+// q8_selftest_sqrt_div); the callers use it for v in [kSqrtMinV, kDivMaxV].
+constexpr float kSqrtMinV = 0x1p-100f;
+
+__device__ __forceinline__ float rsqrt_approx(float v)
+{
+    float y;
+    asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(v));
+    return y;
+}
+
+__device__ __forceinline__ float2 sqrt2_rn(float2 v)
+{
+    const float2 y = make_float2(rsqrt_approx(v.x), rsqrt_approx(v.y));
+    const float2 s0 = __fmul2_rn(v, y);
+    const float2 h = __fmul2_rn(make_float2(0.5f, 0.5f), y);
+    const float2 r = __ffma2_rn(neg2(s0), s0, v);
+    return __ffma2_rn(r, h, s0);
+}
+
+// The same ratio with the packed division (only inside the bounds above).
+__device__ __forceinline__ float2 ratio2_fast(const Scalars& s, float2 m, float2 root)
+{
+    return div2_rn(m, __fadd2_rn(root, splat(s.eps_t)));
 }
 
 // The parameter update of a pair given sqrt(v): p*decay - a_t*(m/(sqrt(v)+eps_t)).
@@ -226,6 +298,13 @@ __device__ __forceinline__ uint32_t pack4(uint32_t q0, uint32_t q1, uint32_t q2,
 __device__ __forceinline__ uint32_t byte_of(uint32_t w, int j) { return __byte_perm(w, 0u, 0x4440 | j); }
 
 // ---------------------------------------------------------------- misc
+__device__ __forceinline__ float min3(float a, float b, float c)
+{
+    float r;
+    asm("min.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ float max3(float a, float b, float c)
 {
     float r;

@@ -65,6 +65,7 @@ struct Scalars {
     float b1, omb1, b2, omb2, eps_t, step_size, decay;
     PhiloxKey key;
     int32_t sr;
+    int32_t fast_div;          // eps_t in [2^-100, 2^20]: the packed division may be used
 };
 
 // Tensor lists travel as kernel parameters (no device allocation, no copy):
@@ -170,6 +171,7 @@ cudaError_t launch_quantize(const float* x, uint8_t* codes, float* absmax, int64
                             const DevTables* tab, cudaStream_t st);
 cudaError_t launch_dequantize(const uint8_t* codes, const float* absmax, float* x, int64_t n,
                               int kind, const DevTables* tab, cudaStream_t st);
+cudaError_t launch_selftest_sqrt_div(uint64_t* counts, cudaStream_t st);
 cudaError_t launch_philox_fill(const PhiloxKey& key, uint32_t stream_id, uint64_t offset, int64_t n,
                                uint16_t* out, cudaStream_t st);
 

@@ -84,6 +84,19 @@ __device__ __forceinline__ float absmax4(float2 a, float2 b)
     return fmaxf(max3(fabsf(a.x), fabsf(a.y), fabsf(b.x)), fabsf(b.y));
 }
 
+// Smallest of four values (min ignores a NaN operand).
+__device__ __forceinline__ float min4(float2 a, float2 b)
+{
+    return fminf(min3(a.x, a.y, b.x), b.y);
+}
+
+// Smallest magnitude of four values (min ignores a NaN operand, as max does;
+// a NaN m then gives a NaN quotient on either division path).
+__device__ __forceinline__ float absmin4(float2 a, float2 b)
+{
+    return fminf(min3(fabsf(a.x), fabsf(a.y), fabsf(b.x)), fabsf(b.y));
+}
+
 // Shared-memory view of the staged tables and the reduction scratch.
 struct Smem8 {
     const float* cs;
@@ -151,17 +164,7 @@ __device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int
         v[k] = __fmul2_rn(make_float2(sm.cu[byte_of(vw, b0)], sm.cu[byte_of(vw, b0 + 1)]), Vold);
         moments2(s, bf16x2(f.g[k]), m[k], v[k]);
     }
-#pragma unroll
-    for (int k = 0; k < 8; ++k) {
-        const float2 root = make_float2(__fsqrt_rn(v[k].x), __fsqrt_rn(v[k].y));
-        po[k] = round2<SR>(param2(s, bf16x2(f.p[k]), m[k], root), r[k]);
-    }
-
-    if constexpr (FULL) {
-        // the parameters do not wait for the block absmax: store them now
-        st_stream16(d.p + i0, make_uint4(po[0], po[1], po[2], po[3]));
-        st_stream16(d.p + i0 + 8, make_uint4(po[4], po[5], po[6], po[7]));
-    } else {
+    if constexpr (!FULL) {
         // padding elements do not count in the block absmax
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -169,12 +172,36 @@ __device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int
             if (2 * k + 1 >= rem) { m[k].y = 0.0f; v[k].y = 0.0f; }
         }
     }
-
-    // block absmax of the new moments
+    // this thread's share of the block absmax of the new moments; with the
+    // smallest |m| it also decides whether the packed division is exact here
     const float lm = fmaxf(fmaxf(absmax4(m[0], m[1]), absmax4(m[2], m[3])),
                            fmaxf(absmax4(m[4], m[5]), absmax4(m[6], m[7])));
     const float lv = fmaxf(fmaxf(absmax4(v[0], v[1]), absmax4(v[2], v[3])),
                            fmaxf(absmax4(v[4], v[5]), absmax4(v[6], v[7])));
+    bool fast = false;
+    if constexpr (FULL) {
+        const float lo = fminf(fminf(absmin4(m[0], m[1]), absmin4(m[2], m[3])),
+                               fminf(absmin4(m[4], m[5]), absmin4(m[6], m[7])));
+        const float lov = fminf(fminf(min4(v[0], v[1]), min4(v[2], v[3])), fminf(min4(v[4], v[5]), min4(v[6], v[7])));
+        fast = s.fast_div && lo >= kDivMinM && lm <= kDivMaxM && lv <= kDivMaxV && lov >= kSqrtMinV;
+    }
+    if (fast) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            po[k] = round2<SR>(step2(s, bf16x2(f.p[k]), ratio2_fast(s, m[k], sqrt2_rn(v[k]))), r[k]);
+    } else {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const float2 root = make_float2(__fsqrt_rn(v[k].x), __fsqrt_rn(v[k].y));
+            po[k] = round2<SR>(param2(s, bf16x2(f.p[k]), m[k], root), r[k]);
+        }
+    }
+
+    if constexpr (FULL) {
+        // the parameters do not wait for the block absmax: store them now
+        st_stream16(d.p + i0, make_uint4(po[0], po[1], po[2], po[3]));
+        st_stream16(d.p + i0 + 8, make_uint4(po[4], po[5], po[6], po[7]));
+    }
     // non-negative floats order like their bit patterns
     const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(lm));
     const uint32_t wv = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(lv));

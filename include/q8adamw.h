@@ -226,6 +226,26 @@ int q8_philox_fill(uint64_t seed, uint32_t step, uint32_t stream_id, uint64_t of
                    int64_t n, uint16_t* out, q8_stream_t stream);
 
 /*
+ * Self-test of the packed square root and division the AdamW steps use where
+ * they are exact, run on the device against CUDA's IEEE operations.  The
+ * division is Markstein's correction (IBM J. Res. Dev. 34(1), 1990) with
+ * y = RN(1/d) from the approximate reciprocal and one Newton-Raphson step;
+ * the square root is the approximate reciprocal square root with one
+ * Newton-Raphson (Heron) correction.
+ *   counts[0] = d values whose y differs from __frcp_rn(d), over every
+ *               positive normal d with a normal reciprocal (counts[1] of them);
+ *   counts[2] = pairs (m, d) whose quotient differs from __fdiv_rn(m, d), over
+ *               counts[3] seeded pseudo-random pairs spanning the bounds inside
+ *               which the steps use it (2^-90 <= |m| <= 2^26,
+ *               2^-100 <= d <= 2^21), both signs of m;
+ *   counts[4] = v values whose square root differs from __fsqrt_rn(v), over
+ *               every normal v >= 2^-100 (counts[5] of them).
+ * counts: device uint64[6] (8-byte aligned), overwritten.  Takes about a
+ * second on one GPU.
+ */
+int q8_selftest_sqrt_div(uint64_t* counts, q8_stream_t stream);
+
+/*
  * One-time set-up of the current device: uploads the codebooks and search
  * tables and waits for the copy (a device-wide synchronisation).  Every
  * other entry point calls it on first use; call it yourself before capturing
@@ -237,7 +257,7 @@ int q8_prepare_device(void);
 const char* q8_last_error(void);
 
 /* ABI version: bumped on any change of a signature or struct. */
-int q8_abi_version(void);   /* 3 */
+int q8_abi_version(void);   /* 4 */
 
 #ifdef __cplusplus
 }

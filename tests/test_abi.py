@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version(lib):
-    assert q8.q8_abi_version() == 3
+    assert q8.q8_abi_version() == 4
 
 
 @pytest.mark.parametrize("kind", [q8.SIGNED, q8.UNSIGNED])
@@ -111,6 +111,8 @@ def test_codec_validation(lib):
     assert lib.q8_blockwise_quantize(None, None, None, 0, 0, None) == 0
     assert lib.q8_blockwise_quantize(0x1000, 0x2000, 0x3000, -5, 0, None) == -2
     assert lib.q8_philox_fill(0, 1, 0, 0, 10, 0x1001, None) == -3
+    assert lib.q8_selftest_sqrt_div(None, None) == -1
+    assert lib.q8_selftest_sqrt_div(0x1004, None) == -3
     assert lib.q8_codebook_init(0, None) == -1
     assert lib.q8_codebook_init(7, (C.c_float * 256)()) == -4
 
