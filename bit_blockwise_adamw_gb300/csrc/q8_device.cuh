@@ -154,6 +154,18 @@ __device__ __forceinline__ float2 recip2(float2 d)
     return __ffma2_rn(y0, e, y0);
 }
 
+// RN(1/x) of one value: the Newton-corrected approximation where it is exact
+// (x normal with a normal reciprocal), the IEEE reciprocal elsewhere (0, tiny,
+// huge and non-finite x).  Used once per block, so the branch is uniform.
+__device__ __forceinline__ float recip_rn(float x)
+{
+    if (x >= 0x1p-126f && x < 0x1p126f) {
+        const float y0 = rcp_approx(x);
+        return __fmaf_rn(y0, __fmaf_rn(-x, y0, 1.0f), y0);
+    }
+    return __frcp_rn(x);
+}
+
 // RN(m/d) of a pair inside the bounds above.
 __device__ __forceinline__ float2 div2_rn(float2 m, float2 d)
 {

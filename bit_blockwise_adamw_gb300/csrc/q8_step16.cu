@@ -81,11 +81,28 @@ __global__ void __launch_bounds__(kThreads, 4) step16_kernel(const __grid_consta
             v[k] = bf16x2(vw[k]);
             moments2(s, bf16x2(gw[k]), m[k], v[k]);
         }
+        // the packed square root and division where they are exact (bounds in
+        // q8_device.cuh); padding elements of a ragged tail are zero and send
+        // that thread to the IEEE path
+        const float lo = fminf(min3(fabsf(m[0].x), fabsf(m[0].y), fabsf(m[1].x)),
+                               min3(fabsf(m[1].y), fabsf(m[2].x), fminf(fabsf(m[2].y), fminf(fabsf(m[3].x), fabsf(m[3].y)))));
+        const float hi = fmaxf(max3(fabsf(m[0].x), fabsf(m[0].y), fabsf(m[1].x)),
+                               max3(fabsf(m[1].y), fabsf(m[2].x), fmaxf(fabsf(m[2].y), fmaxf(fabsf(m[3].x), fabsf(m[3].y)))));
+        const float vlo = fminf(min3(v[0].x, v[0].y, v[1].x), min3(v[1].y, v[2].x, fminf(v[2].y, fminf(v[3].x, v[3].y))));
+        const float vhi = fmaxf(max3(v[0].x, v[0].y, v[1].x), max3(v[1].y, v[2].x, fmaxf(v[2].y, fmaxf(v[3].x, v[3].y))));
+        if (s.fast_div && lo >= kDivMinM && hi <= kDivMaxM && vlo >= kSqrtMinV && vhi <= kDivMaxV) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                po[k] = round2<SR>(step2(s, bf16x2(pw[k]), ratio2_fast(s, m[k], sqrt2_rn(v[k]))), rp[k]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 root = make_float2(__fsqrt_rn(v[k].x), __fsqrt_rn(v[k].y));
+                po[k] = round2<SR>(param2(s, bf16x2(pw[k]), m[k], root), rp[k]);
+            }
+        }
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const float2 root = make_float2(__fsqrt_rn(v[k].x), __fsqrt_rn(v[k].y));
-            const float2 pn = param2(s, bf16x2(pw[k]), m[k], root);
-            po[k] = round2<SR>(pn, rp[k]);
             mo[k] = round2<SR>(m[k], rm[k]);
             vo[k] = round2<SR>(v[k], rv[k]);
         }

@@ -217,7 +217,7 @@ __device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int
     // the saturating multiply maps NaN to +0, whose codes are the zero codes
     // (127 signed, whatever the sign of m; 0 unsigned).
     uint32_t mo[4], vo[4];
-    const float im = __frcp_rn(M), iv = __frcp_rn(V);
+    const float im = recip_rn(M), iv = recip_rn(V);
 #pragma unroll
     for (int k = 0; k < 8; k += 2) {
         mo[k >> 1] = pack4(code_signed_scaled(m[k].x, im, sm.cell_s), code_signed_scaled(m[k].y, im, sm.cell_s),
