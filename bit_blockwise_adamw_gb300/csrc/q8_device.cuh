@@ -254,36 +254,29 @@ __device__ __forceinline__ uint32_t sat_mul_bits(float x, float s)
     return __float_as_uint(r);
 }
 
-// a: bits of min(|y|, 1); neg: all ones when y < 0, else zero.  The table
-// counts, per magnitude cell, the positive midpoints (indices 127..253) below
-// the cell and holds the low bits of the one inside it.  By the odd symmetry
-// of the signed book, y > 0 takes code 127 + #{positive midpoints < |y|} and
-// y < 0 takes 127 - #{positive midpoints <= |y|}; the comparison key carries
-// 0xFF00 in its low half for y < 0 (above any base count, below the marker of
-// a cell without a midpoint), which turns "<" into "<=".
-__device__ __forceinline__ uint32_t signed_key(uint32_t a, uint32_t neg)
-{
-    // bytes (high to low): a.b1, a.b0, neg.b0, and the sign of a.b3 (0: a >= 0)
-    uint32_t k;
-    asm("prmt.b32 %0, %1, %2, 0x104B;" : "=r"(k) : "r"(a), "r"(neg));
-    return k;
-}
-
-__device__ __forceinline__ uint32_t code_signed_mag(uint32_t a, uint32_t neg, const uint32_t* cells)
-{
-    const int cell = __viaddmax_s32(static_cast<int>(a >> kCellShift), kSignedCellBias, 0);
-    const uint32_t e = cells[cell];
-    const uint32_t key = signed_key(a, neg);             // (a << 16) | (neg & 0xFF00)
-    const uint32_t c = e + (key > e ? 1u : 0u);
-    return 127u + ((c ^ neg) - neg);
-}
-
-// m scaled by inv (= RN(1/absmax) > 0): code in the signed book.
+// m scaled by inv (= RN(1/absmax) > 0): code in the signed book.  a holds the
+// bits of min(|m|*inv, 1) (one saturating multiply).  The table counts, per
+// magnitude cell, the positive midpoints (indices 127..253) below the cell and
+// holds the low bits of the one inside it.  By the odd symmetry of the signed
+// book, m > 0 takes code 127 + #{positive midpoints < |y|} and m < 0 takes
+// 127 - #{positive midpoints <= |y|}: the comparison key carries 0xFF00 in its
+// low half for m < 0 (above any base count, below the marker of a cell
+// without a midpoint), which turns "<" into "<=", and the count is applied
+// with one integer multiply-add by s = +1 or -1.  Only the low byte of the
+// result is the code.
 __device__ __forceinline__ uint32_t code_signed_scaled(float m, float inv, const uint32_t* cells)
 {
     const uint32_t a = sat_mul_bits(fabsf(m), inv);
-    const uint32_t neg = static_cast<uint32_t>(static_cast<int>(__float_as_uint(m)) >> 31);
-    return code_signed_mag(a, neg, cells);
+    const uint32_t mb = __float_as_uint(m);
+    const int cell = __viaddmax_s32(static_cast<int>(a >> kCellShift), kSignedCellBias, 0);
+    const uint32_t e = cells[cell];
+    // key bytes, high to low: a.b1, a.b0, the sign of m replicated, the sign of
+    // a replicated (0, as a >= 0): (a << 16) | (m < 0 ? 0xFF00 : 0)
+    uint32_t key;
+    asm("prmt.b32 %0, %1, %2, 0x10FB;" : "=r"(key) : "r"(a), "r"(mb));
+    const uint32_t c = e + (key > e ? 1u : 0u);
+    const uint32_t s = static_cast<uint32_t>(static_cast<int>(mb) >> 31) | 1u;
+    return c * s + 127u;
 }
 
 // a: bits of a value in [0, 1] (unsigned book).

@@ -163,7 +163,7 @@ __device__ __forceinline__ void block1(const Scalars1& s, const Desc8& d, int lb
 
     // absmax 0 needs no branch: m * RN(1/0) saturates to +0, the zero code 127
     uint32_t mo[4];
-    const float im = __frcp_rn(M);
+    const float im = recip_rn(M);
 #pragma unroll
     for (int k = 0; k < 8; k += 2) {
         mo[k >> 1] = pack4(code_signed_scaled(m[k].x, im, tb->cell_s), code_signed_scaled(m[k].y, im, tb->cell_s),
