@@ -223,12 +223,6 @@ __device__ __forceinline__ float2 param2(const Scalars& s, float2 p, float2 m, f
     return step2(s, p, ratio2(s, m, root));
 }
 
-__device__ __forceinline__ float2 adamw2(const Scalars& s, float2 g, float2 p, float2& m, float2& v)
-{
-    moments2(s, g, m, v);
-    return param2(s, p, m, make_float2(__fsqrt_rn(v.x), __fsqrt_rn(v.y)));
-}
-
 // Scalar form (same rounding), for the small-tensor kernel.
 __device__ __forceinline__ float adamw(const Scalars& s, float g, float p, float& m, float& v)
 {

@@ -6,6 +6,8 @@
 // Pure streaming: 8 bytes read and 6 written per element.  A persistent grid
 // walks contiguous ranges of 2048-element blocks; each thread owns eight
 // contiguous elements and draws three independent Philox streams (p, m, v).
+// The square root and division take the packed exact path when all of a
+// thread's eight elements lie inside its bounds (q8_device.cuh).
 #include "q8_device.cuh"
 
 namespace q8 {

@@ -13,8 +13,9 @@
 // of its 128 threads owns sixteen contiguous elements: 16-byte streaming
 // loads of grad, param and both code arrays.  The kernel is bound by
 // instruction issue rather than by DRAM, so the loop is written to keep the
-// instruction count down: packed fp32x2 arithmetic, one shared-memory lookup
-// per code, warp reductions with redux.sync, uniform branches only.
+// instruction count down: packed fp32x2 arithmetic (with a packed exact square
+// root and division wherever a thread's values allow it), one shared-memory
+// lookup per code, warp reductions with redux.sync.
 #include "q8_device.cuh"
 
 namespace q8 {
