@@ -9,10 +9,15 @@ offsets) and the union of the ranks' results is bit-identical to one
 unsharded step.  Replicas that each update the whole list draw the same bits
 and stay identical without any exchange.
 
-This module is host-side planning only; the step itself runs in the library.
+This module is host-side planning plus the one exchange a sharded
+(ZeRO-style) data-parallel step needs afterwards: `gather_params` brings every
+rank's updated parameter slices to all ranks with one all-gather of a flat
+buffer (2 bytes per parameter).  The step itself runs in the library.
 """
 from dataclasses import dataclass
 from typing import List, Sequence
+
+import torch
 
 BLOCK = 2048
 SMALL_NUMEL = 4096
@@ -70,3 +75,34 @@ def shard(tensors, world: int, rank: int):
         else:
             out.append(type(t)(t.param, t.grad, m32=t.m32, v32=t.v32, philox_offset=s.philox_offset))
     return out
+
+
+def gather_params(params: Sequence[torch.Tensor], world: int, rank: int, group=None) -> None:
+    """After each rank has stepped its `plan(...)[rank]` slices of `params`
+    (1-D bf16 tensors, one per list entry, on this rank's device), copy every
+    rank's updated slices into every rank's `params`: each rank packs its
+    slices end to end into one buffer, padded to the longest rank's length,
+    and one all_gather of int32 words over `group` (torch.distributed: NCCL on
+    GPUs, gloo on the CPU) exchanges them.  In place; returns when done."""
+    import torch.distributed as dist
+    shards = plan([p.numel() for p in params], world)
+    sizes = [sum(s.count for s in sl) for sl in shards]
+    width = max(sizes) if sizes else 0
+    if width == 0:
+        return
+    width += width & 1                  # exchanged as int32 words (gloo has no int16)
+    dev = params[0].device
+    mine = torch.zeros(width, dtype=torch.int16, device=dev)
+    at = 0
+    for s in shards[rank]:
+        mine[at:at + s.count] = params[s.tensor].view(torch.int16)[s.start:s.start + s.count]
+        at += s.count
+    bufs = [torch.empty(width, dtype=torch.int16, device=dev) for _ in range(world)]
+    dist.all_gather([b.view(torch.int32) for b in bufs], mine.view(torch.int32), group=group)
+    for r, sl in enumerate(shards):
+        if r == rank:
+            continue
+        at = 0
+        for s in sl:
+            params[s.tensor].view(torch.int16)[s.start:s.start + s.count] = bufs[r][at:at + s.count]
+            at += s.count

@@ -146,3 +146,43 @@ def test_gloo_two_ranks_sharded_step(tmp_path):
     got = np.load(os.path.join(tmp_path, "sharded.npz"))
     for i, st in enumerate(whole):
         assert np.array_equal(got["arr_%d" % i], st.param)
+
+
+def _gather_worker(rank, world, port):
+    """Each rank keeps the optimizer state of its own slices only, steps them
+    with the oracle, and all-gathers the updated parameters every step: all
+    ranks end with the unsharded step's parameters."""
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        params, _ = _data(0)
+        views = [torch.from_numpy(p.view(np.int16)).view(torch.bfloat16) for p in params]
+        states = [o.State8.zeros(p, np.zeros_like(p)) for p in params]     # full-size, only own slices used
+        slices = S.plan(SIZES, world)[rank]
+        for t in range(1, 4):
+            _, grads = _data(t)
+            for st, g in zip(states, grads):
+                st.grad = g
+            mine = _oracle_slices(states, slices)
+            o.adamw8bit_sr_step(mine, o.hparams(step=t, seed=11))
+            for s, m in zip(slices, mine):
+                st = states[s.tensor]
+                sl = slice(s.start, s.start + s.count)
+                st.param[sl] = m.param
+                if st.m_codes is not None:
+                    b0, b1 = s.start // 2048, (s.start + s.count + 2047) // 2048
+                    st.m_codes[sl], st.v_codes[sl] = m.m_codes, m.v_codes
+                    st.m_absmax[b0:b1], st.v_absmax[b0:b1] = m.m_absmax, m.v_absmax
+                else:
+                    st.m32[:], st.v32[:] = m.m32, m.v32
+            S.gather_params(views, world, rank)                       # st.param shares memory with views
+        whole, _ = _run(1, 0)
+        for st, w in zip(states, whole):
+            assert np.array_equal(st.param, w.param)
+        dist.barrier()
+    finally:
+        dist.destroy_process_group()
+
+
+def test_gloo_three_ranks_sharded_step_with_param_all_gather():
+    tmp.spawn(_gather_worker, args=(3, _free_port()), nprocs=3, join=True)
