@@ -129,7 +129,7 @@ __device__ __forceinline__ void moments2(const Scalars& s, float2 g, float2& m, 
 // of elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
 // Dev. 34(1), 1990): q0 = RN(m*y), r = RN(m - d*q0) (one fma),
 // q = RN(q0 + r*y) (one fma) is RN(m/d) when y = RN(1/d) and no intermediate
-// leaves the normal range.  Callers use it only inside kDivSafe* bounds and
+// leaves the normal range.  Callers use it only inside the kDiv* bounds and
 // fall back to the IEEE division otherwise.
 constexpr float kDivMinM = 0x1p-90f;      // |m| at least this (and nonzero: the sign of 0)
 constexpr float kDivMaxM = 0x1p26f;       // |m| at most this

@@ -57,6 +57,27 @@ __device__ __forceinline__ float sign1(float c)
     return fabsf(c) > 0.0f ? __uint_as_float((__float_as_uint(c) & 0x80000000u) | 0x3F800000u) : 0.0f;
 }
 
+// sign(c) of a pair on the FMA pipe: for any nonzero c (subnormals included)
+// |c * 2^126 * 2^126| >= 1, so two saturating multiplies give 1 for c > 0 and
+// for -c > 0; their difference is +-1, and 0 for +-0 and NaN (a saturating
+// multiply maps NaN to 0).  Adding +0 turns a -0 difference into +0, the same
+// zero sign1 gives.  Three fewer ALU operations than sign1 for three more on
+// the FMA pipe, which the one-state kernel has to spare.
+__device__ __forceinline__ float sat_mul(float x, float y)
+{
+    float r;
+    asm("mul.rn.sat.f32 %0, %1, %2;" : "=f"(r) : "f"(x), "f"(y));
+    return r;
+}
+
+__device__ __forceinline__ float2 sign2(float2 c)
+{
+    const float2 t = __fmul2_rn(c, splat(0x1p126f));
+    const float2 pos = make_float2(sat_mul(t.x, 0x1p126f), sat_mul(t.y, 0x1p126f));
+    const float2 neg = make_float2(sat_mul(-t.x, 0x1p126f), sat_mul(-t.y, 0x1p126f));
+    return __fadd2_rn(__fadd2_rn(pos, neg2(neg)), splat(0.0f));
+}
+
 // The element update of a pair (fp32, each x*y + z fused).
 template <int OPT>
 __device__ __forceinline__ float2 onestate2(const Scalars1& s, float2 g, float2 p, float2& m)
@@ -67,7 +88,7 @@ __device__ __forceinline__ float2 onestate2(const Scalars1& s, float2 g, float2 
         return __ffma2_rn(splat(s.lr_neg), m, p);
     } else {
         const float2 c = __ffma2_rn(splat(s.a), m, __fmul2_rn(splat(s.oma), g));
-        const float2 u = make_float2(sign1(c.x), sign1(c.y));
+        const float2 u = sign2(c);
         const float2 pn = __ffma2_rn(splat(s.lr_neg), u, __fmul2_rn(p, splat(s.decay)));
         m = __ffma2_rn(splat(s.b), m, __fmul2_rn(splat(s.omb), g));
         return pn;
