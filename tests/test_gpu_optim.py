@@ -100,7 +100,7 @@ def test_front_end_trains_a_linear_model(cuda_device, cls):
     g = torch.Generator(device=cuda_device).manual_seed(3)
     target = torch.randn(64, 256, generator=g, device=cuda_device) / 16
     model = torch.nn.Linear(256, 64, bias=True, dtype=torch.bfloat16, device=cuda_device)
-    lr = 1e-4 if cls is optim.Lion8bitSR else 3e-3
+    lr = 1e-3 if cls is optim.Lion8bitSR else 3e-3
     opt = cls(model.parameters(), lr=lr, weight_decay=0.0, seed=1)
     x = torch.randn(512, 256, generator=g, device=cuda_device)
     y = x @ target.T
