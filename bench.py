@@ -45,6 +45,8 @@ def parse():
                     help="replace the workload by one flat tensor of this many params (profiling)")
     ap.add_argument("--flat-state", default="8bit", choices=["8bit", "bf16"],
                     help="optimizer state of the --flat tensor")
+    ap.add_argument("--rounding", default="stochastic", choices=["stochastic", "nearest"],
+                    help="bf16 writes: stochastic rounding (the method) or round-to-nearest-even")
     ap.add_argument("--optimizer", default="adamw", choices=["adamw", "momentum", "lion"],
                     help="8-bit-state optimizer of the step (adamw is the headline)")
     ap.add_argument("--no-e2e", action="store_true")
@@ -320,15 +322,17 @@ def main():
     numel = wl.numel
     h = dict(wl.hp)
 
+    sr = 1 if args.rounding == "stochastic" else 0
+
     def hp(t):
         if args.optimizer == "momentum":
             return q8.momentum_hparams(lr=h["lr"], momentum=h["beta1"], weight_decay=h["weight_decay"],
-                                       step=t, seed=wl.philox_seed)
+                                       step=t, seed=wl.philox_seed, sr=sr)
         if args.optimizer == "lion":
             return q8.lion_hparams(lr=h["lr"], beta1=h["beta1"], beta2=0.99, weight_decay=h["weight_decay"],
-                                   step=t, seed=wl.philox_seed)
+                                   step=t, seed=wl.philox_seed, sr=sr)
         return q8.hparams(lr=h["lr"], beta1=h["beta1"], beta2=h["beta2"], eps=h["eps"],
-                          weight_decay=h["weight_decay"], step=t, seed=wl.philox_seed)
+                          weight_decay=h["weight_decay"], step=t, seed=wl.philox_seed, sr=sr)
 
     stream = torch.cuda.current_stream(device)
     t = 0
@@ -404,7 +408,8 @@ def main():
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": wl.name, "optimizer": args.optimizer, "params": numel, "tensors": len(wl.tensors),
+            "config": {"workload": wl.name, "optimizer": args.optimizer, "rounding": args.rounding,
+                       "params": numel, "tensors": len(wl.tensors),
                        "blocks": wl.blocks(), "state": wl.state,
                        "bytes_per_step": abytes, "gbs": abytes / (ms_per_step / 1e3) / 1e9,
                        "l2": "inputs larger than L2 (%.1f GB moved per step, no flush)" % (abytes / 1e9),

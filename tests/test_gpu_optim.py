@@ -110,5 +110,5 @@ def test_front_end_trains_a_linear_model(cuda_device, cls):
         loss = (model(x.to(torch.bfloat16)).float() - y).square().mean()
         loss.backward()
         opt.step()
-        losses.append(float(loss))
+        losses.append(float(loss.detach()))
     assert losses[-1] < losses[0] / 10, (losses[0], losses[-1])
