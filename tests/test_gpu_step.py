@@ -245,3 +245,66 @@ def test_sharded_step_equals_unsharded(cuda_device, world):
             assert torch.equal(a.m_absmax, b.m_absmax) and torch.equal(a.v_absmax, b.v_absmax)
         else:
             assert torch.equal(a.m32, b.m32) and torch.equal(a.v32, b.v32)
+
+
+def test_packed_sqrt_division_guard_boundaries(cuda_device):
+    """Blocks whose moments straddle the bounds of the packed exact square root
+    and division (|m| around 2^-90 and 2^26, v around 2^-100 and 2^40), so that
+    within one warp some threads take the packed path and others the IEEE one;
+    every result equals the oracle's, which uses IEEE sqrt and division only."""
+    blocks = [(2.0 ** 27, 1.0), (2.0 ** 25, 2.0 ** 41), (2.0 ** -80, 1e-6), (1e-3, 2.0 ** -95),
+              (2.0 ** -88, 2.0 ** -98), (3.0, 2.0 ** 39), (1e-4, 1e-9), (2.0 ** 20, 2.0 ** 39.9)]
+    nb = len(blocks)
+    n = nb * 2048
+    rng = np.random.default_rng(86)
+    p = (np.asarray(rng.standard_normal(n) * 0.02, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    mc = rng.integers(0, 255, n).astype(np.uint8)
+    vc = rng.integers(0, 256, n).astype(np.uint8)
+    ma = np.array([b[0] for b in blocks], np.float32)
+    va = np.array([b[1] for b in blocks], np.float32)
+    host = o.State8(p.copy(), np.zeros(n, np.uint16), mc.copy(), vc.copy(), ma.copy(), va.copy())
+    dev = cuda_device
+    gpu = q8.Tensor8(torch.from_numpy(p.view(np.int16)).to(dev).view(torch.bfloat16),
+                     torch.zeros(n, dtype=torch.bfloat16, device=dev),
+                     torch.from_numpy(mc).to(dev), torch.from_numpy(vc).to(dev),
+                     torch.from_numpy(ma).to(dev), torch.from_numpy(va).to(dev))
+    for step in range(1, 4):
+        g = (np.asarray(rng.standard_normal(n) * 10.0 ** rng.uniform(-12, 2, n), np.float32)
+             .view(np.uint32) >> 16).astype(np.uint16)
+        host.grad = g
+        gpu.grad = torch.from_numpy(g.view(np.int16)).to(dev).view(torch.bfloat16)
+        h = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=step, seed=21, sr=1)
+        q8.adamw8bit_sr_step([gpu], q8.hparams(**h))
+        o.adamw8bit_sr_step([host], o.hparams(**h))
+        torch.cuda.synchronize()
+        compare_state8(gpu, host, "step %d" % step)
+
+
+def test_bf16_state_guard_boundaries(cuda_device):
+    """BF16 state with moments spread over the bounds of the packed exact
+    square root and division (|m| from 2^-100 to 2^30, v from 2^-110 to 2^45,
+    zeros included): both paths agree with the oracle bit for bit."""
+    n = 64 * 1024 + 40
+    rng = np.random.default_rng(87)
+
+    def bf(x):
+        return (np.asarray(x, np.float32).view(np.uint32) >> 16).astype(np.uint16)
+    p = bf(rng.standard_normal(n) * 0.02)
+    m = bf(rng.choice([-1.0, 1.0], n) * 2.0 ** rng.uniform(-100, 30, n))
+    v = bf(2.0 ** rng.uniform(-110, 45, n))
+    m[::97] = 0
+    v[::89] = 0
+    host = o.State16(p.copy(), np.zeros(n, np.uint16), m.copy(), v.copy())
+    dev = cuda_device
+    t = lambda a: torch.from_numpy(a.view(np.int16)).to(dev).view(torch.bfloat16)
+    gpu = q8.Tensor16(t(p), t(np.zeros(n, np.uint16)), t(m), t(v))
+    for step in range(1, 4):
+        g = bf(rng.standard_normal(n) * 10.0 ** rng.uniform(-12, 2, n))
+        host.grad = g
+        gpu.grad = t(g)
+        h = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=step, seed=22, sr=1)
+        q8.adamw_bf16_sr_step([gpu], q8.hparams(**h))
+        o.adamw_bf16_sr_step([host], o.hparams(**h))
+        torch.cuda.synchronize()
+        for name, a, b in (("param", gpu.param, host.param), ("m", gpu.m, host.m), ("v", gpu.v, host.v)):
+            np.testing.assert_array_equal(u16(a), b, err_msg="%s step %d" % (name, step))
