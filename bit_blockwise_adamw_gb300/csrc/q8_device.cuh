@@ -248,28 +248,57 @@ __device__ __forceinline__ uint32_t sat_mul_bits(float x, float s)
     return __float_as_uint(r);
 }
 
+// Four codes (low bytes of q0..q3) -> one word, q0 in the lowest byte.
+__device__ __forceinline__ uint32_t pack4(uint32_t q0, uint32_t q1, uint32_t q2, uint32_t q3)
+{
+    return __byte_perm(__byte_perm(q0, q1, 0x0040), __byte_perm(q2, q3, 0x0040), 0x5410);
+}
+
 // m scaled by inv (= RN(1/absmax) > 0): code in the signed book.  a holds the
 // bits of min(|m|*inv, 1) (one saturating multiply).  The table counts, per
 // magnitude cell, the positive midpoints (indices 127..253) below the cell and
 // holds the low bits of the one inside it.  By the odd symmetry of the signed
 // book, m > 0 takes code 127 + #{positive midpoints < |y|} and m < 0 takes
-// 127 - #{positive midpoints <= |y|}: the comparison key carries 0xFF00 in its
-// low half for m < 0 (above any base count, below the marker of a cell
-// without a midpoint), which turns "<" into "<=", and the count is applied
-// with one integer multiply-add by s = +1 or -1.  Only the low byte of the
-// result is the code.
-__device__ __forceinline__ uint32_t code_signed_scaled(float m, float inv, const uint32_t* cells)
+// 127 - #{positive midpoints <= |y|}.  count_signed_scaled returns that count
+// (in its low byte): the comparison key carries 0xFF00 in its low half for
+// m < 0 (above any base count, below the marker of a cell without a
+// midpoint), which turns "<" into "<=".  signed_codes4 applies the signs to
+// four counts at once.
+__device__ __forceinline__ uint32_t count_signed_scaled(float m, float inv, const uint32_t* cells)
 {
     const uint32_t a = sat_mul_bits(fabsf(m), inv);
-    const uint32_t mb = __float_as_uint(m);
     const int cell = __viaddmax_s32(static_cast<int>(a >> kCellShift), kSignedCellBias, 0);
     const uint32_t e = cells[cell];
     // key bytes, high to low: a.b1, a.b0, the sign of m replicated, the sign of
     // a replicated (0, as a >= 0): (a << 16) | (m < 0 ? 0xFF00 : 0)
     uint32_t key;
-    asm("prmt.b32 %0, %1, %2, 0x10FB;" : "=r"(key) : "r"(a), "r"(mb));
-    const uint32_t c = e + (key > e ? 1u : 0u);
-    const uint32_t s = static_cast<uint32_t>(static_cast<int>(mb) >> 31) | 1u;
+    asm("prmt.b32 %0, %1, %2, 0x10FB;" : "=r"(key) : "r"(a), "r"(__float_as_uint(m)));
+    return e + (key > e ? 1u : 0u);
+}
+
+// Signed codes of four values from their counts c0..c3 (low bytes) and their
+// signs: byte i is 127 + c_i for m_i >= 0 and 127 - c_i for m_i < 0.  With C
+// the packed counts and S the packed sign bytes (0xFF for m_i < 0), byte i of
+// (C ^ S) - S is +c_i or -c_i, and as every byte of the result lies in
+// [0, 254], the one 32-bit sum 0x7F7F7F7F + (C ^ S) - S has exactly those
+// bytes (no carry or borrow crosses a byte).
+__device__ __forceinline__ uint32_t signed_codes4(uint32_t c0, uint32_t c1, uint32_t c2, uint32_t c3, float m0,
+                                                  float m1, float m2, float m3)
+{
+    const uint32_t C = pack4(c0, c1, c2, c3);
+    uint32_t s01, s23, S;
+    // byte 0 <- sign of byte 3 (m0's top byte) replicated, byte 1 <- sign of byte 7 (m1's)
+    asm("prmt.b32 %0, %1, %2, 0x00FB;" : "=r"(s01) : "r"(__float_as_uint(m0)), "r"(__float_as_uint(m1)));
+    asm("prmt.b32 %0, %1, %2, 0x00FB;" : "=r"(s23) : "r"(__float_as_uint(m2)), "r"(__float_as_uint(m3)));
+    S = __byte_perm(s01, s23, 0x5410);
+    return 0x7F7F7F7Fu + (C ^ S) - S;
+}
+
+// The signed code of one value (low byte of the result).
+__device__ __forceinline__ uint32_t code_signed_scaled(float m, float inv, const uint32_t* cells)
+{
+    const uint32_t c = count_signed_scaled(m, inv, cells);
+    const uint32_t s = static_cast<uint32_t>(static_cast<int>(__float_as_uint(m)) >> 31) | 1u;
     return c * s + 127u;
 }
 
@@ -285,12 +314,6 @@ __device__ __forceinline__ uint32_t code_unsigned_mag(uint32_t a, const uint32_t
 __device__ __forceinline__ uint32_t code_unsigned_scaled(float v, float inv, const uint32_t* cells)
 {
     return code_unsigned_mag(sat_mul_bits(v, inv), cells);
-}
-
-// Four codes (low bytes of q0..q3) -> one word, q0 in the lowest byte.
-__device__ __forceinline__ uint32_t pack4(uint32_t q0, uint32_t q1, uint32_t q2, uint32_t q3)
-{
-    return __byte_perm(__byte_perm(q0, q1, 0x0040), __byte_perm(q2, q3, 0x0040), 0x5410);
 }
 
 // Byte j (0..3) of w, zero-extended.

@@ -187,9 +187,10 @@ __device__ __forceinline__ void block1(const Scalars1& s, const Desc8& d, int lb
     const float im = recip_rn(M);
 #pragma unroll
     for (int k = 0; k < 8; k += 2) {
-        mo[k >> 1] = pack4(code_signed_scaled(m[k].x, im, tb->cell_s), code_signed_scaled(m[k].y, im, tb->cell_s),
-                           code_signed_scaled(m[k + 1].x, im, tb->cell_s),
-                           code_signed_scaled(m[k + 1].y, im, tb->cell_s));
+        mo[k >> 1] = signed_codes4(count_signed_scaled(m[k].x, im, tb->cell_s), count_signed_scaled(m[k].y, im, tb->cell_s),
+                                   count_signed_scaled(m[k + 1].x, im, tb->cell_s),
+                                   count_signed_scaled(m[k + 1].y, im, tb->cell_s), m[k].x, m[k].y, m[k + 1].x,
+                                   m[k + 1].y);
     }
     if constexpr (FULL) {
         st_stream16(d.mq + i0, make_uint4(mo[0], mo[1], mo[2], mo[3]));
@@ -219,12 +220,16 @@ __global__ void __launch_bounds__(kT1, 8) step1_kernel(const __grid_constant__ S
     const int begin = static_cast<int>((static_cast<int64_t>(blockIdx.x) * a.nblocks) / gridDim.x);
     const int end = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * a.nblocks) / gridDim.x);
     int ti = begin < end ? find_tensor1(a.blk_start, a.nt, begin) : 0;
-    for (int gb = begin, it = 0; gb < end; ++gb) {
+    // tensor by tensor: the descriptor and the tensor's block range are read
+    // once per tensor; a partial last block is the tail kernel's
+    for (int gb = begin, it = 0; gb < end;) {
         while (gb >= a.blk_start[ti + 1]) ++ti;
         const Desc8& d = a.d[ti];
-        const int lb = gb - a.blk_start[ti];
-        if (partial1(d, lb)) continue;
-        block1<OPT, SR, true>(a.s, d, lb, it++, tb, red);
+        const int base = a.blk_start[ti];
+        const int next = a.blk_start[ti + 1];
+        const int full_end = min(min(end, next), base + static_cast<int>(d.n / kBlock));
+        for (; gb < full_end; ++gb) block1<OPT, SR, true>(a.s, d, gb - base, it++, tb, red);
+        gb = min(end, next);
     }
 }
 

@@ -246,9 +246,10 @@ __device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int
     const float im = recip_rn(M), iv = recip_rn(V);
 #pragma unroll
     for (int k = 0; k < 8; k += 2) {
-        mo[k >> 1] = pack4(code_signed_scaled(m[k].x, im, sm.cell_s), code_signed_scaled(m[k].y, im, sm.cell_s),
-                           code_signed_scaled(m[k + 1].x, im, sm.cell_s),
-                           code_signed_scaled(m[k + 1].y, im, sm.cell_s));
+        mo[k >> 1] = signed_codes4(count_signed_scaled(m[k].x, im, sm.cell_s), count_signed_scaled(m[k].y, im, sm.cell_s),
+                                   count_signed_scaled(m[k + 1].x, im, sm.cell_s),
+                                   count_signed_scaled(m[k + 1].y, im, sm.cell_s), m[k].x, m[k].y, m[k + 1].x,
+                                   m[k + 1].y);
         vo[k >> 1] = pack4(code_unsigned_scaled(v[k].x, iv, sm.cell_u), code_unsigned_scaled(v[k].y, iv, sm.cell_u),
                            code_unsigned_scaled(v[k + 1].x, iv, sm.cell_u),
                            code_unsigned_scaled(v[k + 1].y, iv, sm.cell_u));
@@ -273,6 +274,8 @@ __device__ __forceinline__ bool is_partial(const Desc8& d, int lb)
 
 // The hot kernel: every full block of the launch's list.  Partial last blocks
 // are left to step8_tail_kernel, so this loop carries no ragged-tail code.
+// Each CTA takes a contiguous range of the list's blocks (end to end over the
+// tensors).
 template <bool SR>
 __global__ void __launch_bounds__(kT8, 7) step8_kernel(const __grid_constant__ Step8Args a)
 {
@@ -282,27 +285,38 @@ __global__ void __launch_bounds__(kT8, 7) step8_kernel(const __grid_constant__ S
     const int begin = static_cast<int>((static_cast<int64_t>(blockIdx.x) * a.nblocks) / gridDim.x);
     const int end = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * a.nblocks) / gridDim.x);
     int ti = begin < end ? find_tensor(a.blk_start, a.nt, begin) : 0;
-    // L2 prefetch cursor: thread 0 keeps the inputs of the block two ahead in
-    // flight (one, four or six ahead, or none, measured slower).
+    // L2 prefetch: thread 0 keeps the inputs of the block two ahead in flight
+    // (one, three, four or six ahead, or none, measured slower)
     constexpr int kAhead = 2;
-    int pb = begin, tp = ti;
     if (threadIdx.x == 0) {
-        for (; pb < end && pb < begin + kAhead; ++pb) {
-            while (pb >= a.blk_start[tp + 1]) ++tp;
-            prefetch_block(a.d[tp], pb - a.blk_start[tp]);
+        int tq = ti;
+        for (int pg = begin; pg < end && pg < begin + kAhead; ++pg) {
+            while (pg >= a.blk_start[tq + 1]) ++tq;
+            prefetch_block(a.d[tq], pg - a.blk_start[tq]);
         }
     }
-    for (int gb = begin, it = 0; gb < end; ++gb) {
-        if (threadIdx.x == 0 && pb < end) {
-            while (pb >= a.blk_start[tp + 1]) ++tp;
-            prefetch_block(a.d[tp], pb - a.blk_start[tp]);
-            ++pb;
-        }
+    // Tensor by tensor: the descriptor and the tensor's block range are read
+    // once per tensor, not once per block.
+    for (int gb = begin, it = 0; gb < end;) {
         while (gb >= a.blk_start[ti + 1]) ++ti;
         const Desc8& d = a.d[ti];
-        const int lb = gb - a.blk_start[ti];
-        if (is_partial(d, lb)) continue;                 // uniform across the CTA
-        block_step<SR, true>(a.s, d, lb, it++, sm);
+        const int base = a.blk_start[ti];
+        const int next = a.blk_start[ti + 1];
+        const int full_end = min(min(end, next), base + static_cast<int>(d.n / kBlock));
+        for (; gb < full_end; ++gb) {
+            if (threadIdx.x == 0 && gb + kAhead < end) {
+                const int pg = gb + kAhead;
+                if (pg < next) {
+                    prefetch_block(d, pg - base);
+                } else {
+                    int tq = ti + 1;
+                    while (pg >= a.blk_start[tq + 1]) ++tq;
+                    prefetch_block(a.d[tq], pg - a.blk_start[tq]);
+                }
+            }
+            block_step<SR, true>(a.s, d, gb - base, it++, sm);
+        }
+        gb = min(end, next);                             // a partial last block is the tail kernel's
     }
 }
 
