@@ -28,6 +28,28 @@ struct Tables1 {               // the part of DevTables this kernel stages
 static_assert(sizeof(Tables1) % 16 == 0, "staged 16 bytes at a time");
 constexpr int kSmem1 = static_cast<int>(sizeof(Tables1)) + 2 * kW1 * 4;
 
+// Ask the L2 to fetch [p, p + bytes) from DRAM now (a hint, never waited for);
+// bytes a multiple of 16.
+__device__ __forceinline__ void prefetch_l2_1(const void* p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Prefetch the inputs of local block `lb` (grad, param, codes), clipped to
+// whole 16-byte chunks inside the tensor.
+__device__ __forceinline__ void prefetch_block1(const Desc8& d, int lb)
+{
+    const int64_t first = static_cast<int64_t>(lb) * kBlock;
+    const int64_t n = d.n - first < kBlock ? d.n - first : kBlock;
+    const uint32_t b16 = static_cast<uint32_t>(n * 2) & ~15u;
+    const uint32_t b8 = static_cast<uint32_t>(n) & ~15u;
+    if (b16) {
+        prefetch_l2_1(d.g + first, b16);
+        prefetch_l2_1(d.p + first, b16);
+    }
+    if (b8) prefetch_l2_1(d.mq + first, b8);
+}
+
 __device__ __forceinline__ int find_tensor1(const int32_t* start, int nt, int gb)
 {
     int lo = 0, hi = nt;
@@ -220,6 +242,16 @@ __global__ void __launch_bounds__(kT1, 8) step1_kernel(const __grid_constant__ S
     const int begin = static_cast<int>((static_cast<int64_t>(blockIdx.x) * a.nblocks) / gridDim.x);
     const int end = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * a.nblocks) / gridDim.x);
     int ti = begin < end ? find_tensor1(a.blk_start, a.nt, begin) : 0;
+    // L2 prefetch: thread 0 keeps the inputs of the next block in flight (two
+    // ahead measured slower)
+    constexpr int kAhead = 1;
+    if (threadIdx.x == 0) {
+        int tq = ti;
+        for (int pg = begin; pg < end && pg < begin + kAhead; ++pg) {
+            while (pg >= a.blk_start[tq + 1]) ++tq;
+            prefetch_block1(a.d[tq], pg - a.blk_start[tq]);
+        }
+    }
     // tensor by tensor: the descriptor and the tensor's block range are read
     // once per tensor; a partial last block is the tail kernel's
     for (int gb = begin, it = 0; gb < end;) {
@@ -228,7 +260,19 @@ __global__ void __launch_bounds__(kT1, 8) step1_kernel(const __grid_constant__ S
         const int base = a.blk_start[ti];
         const int next = a.blk_start[ti + 1];
         const int full_end = min(min(end, next), base + static_cast<int>(d.n / kBlock));
-        for (; gb < full_end; ++gb) block1<OPT, SR, true>(a.s, d, gb - base, it++, tb, red);
+        for (; gb < full_end; ++gb) {
+            if (threadIdx.x == 0 && gb + kAhead < end) {
+                const int pg = gb + kAhead;
+                if (pg < next) {
+                    prefetch_block1(d, pg - base);
+                } else {
+                    int tq = ti + 1;
+                    while (pg >= a.blk_start[tq + 1]) ++tq;
+                    prefetch_block1(a.d[tq], pg - a.blk_start[tq]);
+                }
+            }
+            block1<OPT, SR, true>(a.s, d, gb - base, it++, tb, red);
+        }
         gb = min(end, next);
     }
 }
