@@ -28,11 +28,14 @@ def pool():
     p.join()
 
 
-def _run_full(wl, device, steps=None, sr=1, offsets=None, split=None, grad_hook=None):
+def _run_full(wl, device, steps=None, sr=1, offsets=None, split=None, grad_hook=None, param_hook=None):
     """Run `wl` on both sides for `steps`, comparing everything after each step
-    (`grad_hook(step, grads)` may edit the step's gradients in place first)."""
+    (`grad_hook(step, grads)` may edit the step's gradients in place first,
+    `param_hook(params)` the initial parameters)."""
     steps = steps or wl.steps
     params = W.init_params(wl, device)
+    if param_hook:
+        param_hook(params)
     gpu = gpu_states8(params, offsets)
     host = host_states8([u16(p) for p in params], offsets)
     for step in range(1, steps + 1):
@@ -85,6 +88,34 @@ def test_zero_gradient_blocks(cuda_device):
         if step >= 3:
             grads[3].zero_()                            # zero after nonzero steps
     _run_full(wl, cuda_device, grad_hook=hook)
+
+
+def test_negative_zero_moments_and_params(cuda_device):
+    """Signed zeros through the whole step, with beta1 = 0 so that the new
+    first moment is 0*m + g.  Elements 0 mod 4 get a -0 gradient every step:
+    their m is +0 (+0 + -0), so where the parameter starts at -0 (every third
+    element) the update is -0*decay - a*(+0/d) = -0, kept step after step.
+    Elements 2 mod 4 get a -0 gradient on even steps: where the old m was
+    negative the new m is -0, which must take the zero code 127 like +0 and
+    the IEEE quotient -0/d = -0.  8-bit blocks, a partial block and the
+    fp32-state path."""
+    wl = W.custom("negzero", [4 * 2048, 2048 * 2 + 300, 3000], steps=4, data_seed=95, hp={"beta1": 0.0})
+
+    def params_hook(params):
+        for p in params:
+            p.view(torch.int16)[::3] = -32768               # bf16 -0 (0x8000)
+
+    def hook(step, grads):
+        for g in grads:
+            g.view(torch.int16)[::4] = -32768
+            if step % 2 == 0:
+                g.view(torch.int16)[2::4] = -32768
+    gpu, host = _run_full(wl, cuda_device, grad_hook=hook, param_hook=params_hook)
+    # the cases are live: -0 parameters survive, and zero codes sit in blocks
+    # whose absmax is nonzero
+    for t in host:
+        assert int((t.param == 0x8000).sum()) > 0
+    assert bool((gpu[0].m_codes == 127).any()) and bool((gpu[0].m_absmax > 0).all())
 
 
 def test_explicit_misaligned_offsets(cuda_device):
