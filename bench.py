@@ -433,7 +433,7 @@ def run_e2e(args, wl, states, step_fn, hp, t, device, world, barrier):
     one chunk's grads ahead of the compute stream).  Which is faster depends
     on the host link: concurrent H2D + D2H reached 343 GB/s on one GB300 machine
     and 99 GB/s on another, against about 200 GB/s one direction at a time.
-    One untimed step of each picks the schedule for the timed steps."""
+    Two untimed steps of each pick the schedule for the timed steps."""
     import bit_blockwise_adamw_gb300 as q8
     from bit_blockwise_adamw_gb300 import workloads as W
     offs = W.philox_offsets(wl)
@@ -503,16 +503,19 @@ def run_e2e(args, wl, states, step_fn, hp, t, device, world, barrier):
         barrier()
         return time.perf_counter() - t0
 
+    # Each trial runs two back-to-back steps, so that the copies of one step
+    # overlap those of the next as in the timed run (a single step from idle
+    # never runs both directions at once for long).
     tt = t + 1
     timed(step_duplex, tt, 1)                  # warm-up
-    d_duplex = timed(step_duplex, tt + 1, 1)
-    d_serial = timed(step_serial, tt + 2, 1)
+    d_duplex = timed(step_duplex, tt + 1, 2) / 2
+    d_serial = timed(step_serial, tt + 3, 2) / 2
     if world > 1:
         tt2 = torch.tensor([d_duplex, d_serial], device=device)
         torch.distributed.all_reduce(tt2, op=torch.distributed.ReduceOp.MAX)
         d_duplex, d_serial = (float(x) for x in tt2.tolist())
     mode, fn = ("duplex", step_duplex) if d_duplex <= d_serial else ("serial", step_serial)
-    dt = timed(fn, tt + 3, args.e2e_steps)
+    dt = timed(fn, tt + 5, args.e2e_steps)
     if world > 1:
         tt3 = torch.tensor([dt], device=device)
         torch.distributed.all_reduce(tt3, op=torch.distributed.ReduceOp.MAX)

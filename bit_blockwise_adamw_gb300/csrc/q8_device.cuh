@@ -335,6 +335,13 @@ __device__ __forceinline__ float max3(float a, float b, float c)
 }
 
 
+// Ask the L2 to fetch [p, p + bytes) from DRAM now: a hint that completes
+// asynchronously and is never waited for.  bytes must be a multiple of 16.
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // Streaming loads/stores: every byte of the step is touched once.
 __device__ __forceinline__ uint4 ld_stream16(const void* p)
 {

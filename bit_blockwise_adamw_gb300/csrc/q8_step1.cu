@@ -28,13 +28,6 @@ struct Tables1 {               // the part of DevTables this kernel stages
 static_assert(sizeof(Tables1) % 16 == 0, "staged 16 bytes at a time");
 constexpr int kSmem1 = static_cast<int>(sizeof(Tables1)) + 2 * kW1 * 4;
 
-// Ask the L2 to fetch [p, p + bytes) from DRAM now (a hint, never waited for);
-// bytes a multiple of 16.
-__device__ __forceinline__ void prefetch_l2_1(const void* p, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // Prefetch the inputs of local block `lb` (grad, param, codes), clipped to
 // whole 16-byte chunks inside the tensor.
 __device__ __forceinline__ void prefetch_block1(const Desc8& d, int lb)
@@ -44,10 +37,10 @@ __device__ __forceinline__ void prefetch_block1(const Desc8& d, int lb)
     const uint32_t b16 = static_cast<uint32_t>(n * 2) & ~15u;
     const uint32_t b8 = static_cast<uint32_t>(n) & ~15u;
     if (b16) {
-        prefetch_l2_1(d.g + first, b16);
-        prefetch_l2_1(d.p + first, b16);
+        prefetch_l2(d.g + first, b16);
+        prefetch_l2(d.p + first, b16);
     }
-    if (b8) prefetch_l2_1(d.mq + first, b8);
+    if (b8) prefetch_l2(d.mq + first, b8);
 }
 
 __device__ __forceinline__ int find_tensor1(const int32_t* start, int nt, int gb)

@@ -80,13 +80,6 @@ __device__ __forceinline__ void store_ragged(const Desc8& d, int64_t i0, int64_t
     }
 }
 
-// Ask the L2 to fetch [p, p + bytes) from DRAM now (a hint: it completes
-// asynchronously and is never waited for).  bytes must be a multiple of 16.
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes)
-{
-    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
-}
-
 // Prefetch the inputs of local block `lb` into L2: grad, param and both code
 // arrays, clipped to whole 16-byte chunks inside the tensor.
 __device__ __forceinline__ void prefetch_block(const Desc8& d, int lb)
