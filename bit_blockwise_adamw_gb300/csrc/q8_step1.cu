@@ -127,9 +127,17 @@ __device__ __forceinline__ float onestate(const Scalars1& s, float g, float p, f
 }
 
 // One block; FULL = sixteen valid elements per thread.
+// The L2 prefetch thread 0 issues during a block: the inputs of global block
+// `target` (when `on`), which lies in the current tensor if target < next.
+struct Prefetch1 {
+    const Step1Args* a;
+    int target, next, base, ti;
+    bool on;
+};
+
 template <int OPT, bool SR, bool FULL>
 __device__ __forceinline__ void block1(const Scalars1& s, const Desc8& d, int lb, int it, const Tables1* tb,
-                                       uint32_t* red2)
+                                       uint32_t* red2, const Prefetch1& pf)
 {
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -146,6 +154,16 @@ __device__ __forceinline__ void block1(const Scalars1& s, const Desc8& d, int lb
         gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w; gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
         pw[0] = p0.x; pw[1] = p0.y; pw[2] = p0.z; pw[3] = p0.w; pw[4] = p1.x; pw[5] = p1.y; pw[6] = p1.z; pw[7] = p1.w;
         mc[0] = mq.x; mc[1] = mq.y; mc[2] = mq.z; mc[3] = mq.w;
+        // after this block's own loads are in flight
+        if (threadIdx.x == 0 && pf.on) {
+            if (pf.target < pf.next) {
+                prefetch_block1(d, pf.target - pf.base);
+            } else {
+                int tq = pf.ti + 1;
+                while (pf.target >= pf.a->blk_start[tq + 1]) ++tq;
+                prefetch_block1(pf.a->d[tq], pf.target - pf.a->blk_start[tq]);
+            }
+        }
     } else {
 #pragma unroll
         for (int j = 0; j < 8; ++j) { gw[j] = 0; pw[j] = 0; }
@@ -253,19 +271,8 @@ __global__ void __launch_bounds__(kT1, 8) step1_kernel(const __grid_constant__ S
         const int base = a.blk_start[ti];
         const int next = a.blk_start[ti + 1];
         const int full_end = min(min(end, next), base + static_cast<int>(d.n / kBlock));
-        for (; gb < full_end; ++gb) {
-            if (threadIdx.x == 0 && gb + kAhead < end) {
-                const int pg = gb + kAhead;
-                if (pg < next) {
-                    prefetch_block1(d, pg - base);
-                } else {
-                    int tq = ti + 1;
-                    while (pg >= a.blk_start[tq + 1]) ++tq;
-                    prefetch_block1(a.d[tq], pg - a.blk_start[tq]);
-                }
-            }
-            block1<OPT, SR, true>(a.s, d, gb - base, it++, tb, red);
-        }
+        for (; gb < full_end; ++gb)
+            block1<OPT, SR, true>(a.s, d, gb - base, it++, tb, red, Prefetch1{&a, gb + kAhead, next, base, ti, gb + kAhead < end});
         gb = min(end, next);
     }
 }
@@ -279,7 +286,7 @@ __global__ void __launch_bounds__(kT1) step1_tail_kernel(const __grid_constant__
     extern __shared__ __align__(16) unsigned char smem[];
     const Tables1* tb = stage1(a.tab, smem);
     uint32_t* red = reinterpret_cast<uint32_t*>(smem + sizeof(Tables1));
-    block1<OPT, SR, false>(a.s, d, lb, 0, tb, red);
+    block1<OPT, SR, false>(a.s, d, lb, 0, tb, red, Prefetch1{&a, 0, 0, 0, 0, false});
 }
 
 // fp32-state path: one CTA per tensor (numel < 4096 = 512 threads x 8).

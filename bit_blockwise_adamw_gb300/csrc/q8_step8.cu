@@ -135,12 +135,21 @@ __device__ __forceinline__ Smem8 stage_tables(const DevTables* tab, unsigned cha
     return Smem8{t->cs, t->cu, t->cell_s, t->cell_u, reinterpret_cast<uint2*>(smem + sizeof(DevTables))};
 }
 
+// The L2 prefetch thread 0 issues during a block: the inputs of global block
+// `target` (when `on`), which lies in the current tensor if target < next.
+struct Prefetch {
+    const Step8Args* a;
+    int target, next, base, ti;
+    bool on;
+};
+
 // One 2048-element block of one tensor.  FULL: every thread owns sixteen
 // valid elements (the hot path: vector loads and stores only); otherwise the
 // block is the partial last block of its tensor.  `it` picks the half of the
 // double-buffered reduction scratch.
 template <bool SR, bool FULL>
-__device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int lb, int it, const Smem8& sm)
+__device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int lb, int it, const Smem8& sm,
+                                           const Prefetch& pf)
 {
     const int tid = threadIdx.x;
     const int lane = tid & 31;
@@ -162,6 +171,17 @@ __device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int
         f.p[4] = p1.x; f.p[5] = p1.y; f.p[6] = p1.z; f.p[7] = p1.w;
         f.mc[0] = mq.x; f.mc[1] = mq.y; f.mc[2] = mq.z; f.mc[3] = mq.w;
         f.vc[0] = vq.x; f.vc[1] = vq.y; f.vc[2] = vq.z; f.vc[3] = vq.w;
+        // after this block's own loads are in flight, so that the prefetch's
+        // work hides in their latency instead of delaying them
+        if (threadIdx.x == 0 && pf.on) {
+            if (pf.target < pf.next) {
+                prefetch_block(d, pf.target - pf.base);
+            } else {
+                int tq = pf.ti + 1;
+                while (pf.target >= pf.a->blk_start[tq + 1]) ++tq;
+                prefetch_block(pf.a->d[tq], pf.target - pf.a->blk_start[tq]);
+            }
+        }
     } else {
         load_ragged(d, i0, rem > 0 ? rem : 0, f);
     }
@@ -296,19 +316,8 @@ __global__ void __launch_bounds__(kT8, 7) step8_kernel(const __grid_constant__ S
         const int base = a.blk_start[ti];
         const int next = a.blk_start[ti + 1];
         const int full_end = min(min(end, next), base + static_cast<int>(d.n / kBlock));
-        for (; gb < full_end; ++gb) {
-            if (threadIdx.x == 0 && gb + kAhead < end) {
-                const int pg = gb + kAhead;
-                if (pg < next) {
-                    prefetch_block(d, pg - base);
-                } else {
-                    int tq = ti + 1;
-                    while (pg >= a.blk_start[tq + 1]) ++tq;
-                    prefetch_block(a.d[tq], pg - a.blk_start[tq]);
-                }
-            }
-            block_step<SR, true>(a.s, d, gb - base, it++, sm);
-        }
+        for (; gb < full_end; ++gb)
+            block_step<SR, true>(a.s, d, gb - base, it++, sm, Prefetch{&a, gb + kAhead, next, base, ti, gb + kAhead < end});
         gb = min(end, next);                             // a partial last block is the tail kernel's
     }
 }
@@ -323,7 +332,7 @@ __global__ void __launch_bounds__(kT8) step8_tail_kernel(const __grid_constant__
     if (!is_partial(d, lb)) return;
     extern __shared__ __align__(16) unsigned char smem[];
     const Smem8 sm = stage_tables(a.tab, smem);
-    block_step<SR, false>(a.s, d, lb, 0, sm);
+    block_step<SR, false>(a.s, d, lb, 0, sm, Prefetch{&a, 0, 0, 0, 0, false});
 }
 
 // fp32-state path: one CTA per tensor (numel < 4096 = 512 threads x 8).
