@@ -182,3 +182,84 @@ def test_weight_decay_survives_with_sr_only():
     sigma = np.sqrt(steps * (2.0 ** -8) ** 2 * 0.003 / n)
     assert abs(vals.mean() - expect) < 3 * sigma
     assert vals.mean() < 0.995
+
+
+# An independent restatement of Philox4x32-10 in numpy uint32/uint64
+# arithmetic, written from Salmon et al. (SC'11), section 4: each of the ten
+# rounds multiplies counter words 0 and 2 by the two round multipliers,
+# crosses the halves of the products with words 1 and 3 and the round key,
+# and the key is bumped by the two Weyl constants between rounds.  Vectorised
+# over many counters; used to pin counter word 3, which cuRAND's offset
+# cannot reach (it is non-zero only past 2^35 elements).
+_PHILOX_M = (np.uint64(0xD2511F53), np.uint64(0xCD9E8D57))
+_PHILOX_W = (0x9E3779B9, 0xBB67AE85)
+
+
+def _philox_numpy(ctr, key):
+    c = [np.asarray(ctr[:, i], np.uint64) for i in range(4)]
+    k0, k1 = int(key[0]), int(key[1])
+    mask = np.uint64(0xFFFFFFFF)
+    for _ in range(10):
+        p0 = _PHILOX_M[0] * c[0]
+        p1 = _PHILOX_M[1] * c[2]
+        c = [(p1 >> np.uint64(32)) ^ c[1] ^ np.uint64(k0), p1 & mask,
+             (p0 >> np.uint64(32)) ^ c[3] ^ np.uint64(k1), p0 & mask]
+        k0 = (k0 + _PHILOX_W[0]) & 0xFFFFFFFF
+        k1 = (k1 + _PHILOX_W[1]) & 0xFFFFFFFF
+    return np.stack([x.astype(np.uint32) for x in c], axis=1)
+
+
+def test_philox_numpy_restatement_agrees_with_curand():
+    """The restatement above is itself right where cuRAND reaches (words 0-2)."""
+    seed = 0x0123456789ABCDEF
+    key = (seed & 0xFFFFFFFF, seed >> 32)
+    ctr = np.array([[0, 0, j, 0] for j in range(32)], np.uint64)
+    want = curand_host_words(seed, 0, 4 * 32).reshape(32, 4)
+    assert np.array_equal(_philox_numpy(ctr, key), want)
+
+
+@pytest.mark.parametrize("seed", [0, 0xFFFFFFFFFFFFFFFF, 0x9E3779B97F4A7C15])
+def test_philox_word3_against_numpy_restatement(seed):
+    rng = np.random.default_rng(seed & 0xFFFF)
+    key = np.array([seed & 0xFFFFFFFF, seed >> 32], np.uint64)
+    ctr = rng.integers(0, 2 ** 32, (300, 4), dtype=np.uint64)
+    ctr[:100, 3] = rng.integers(1, 16, 100)          # small non-zero word 3 (E just past 2^35)
+    ctr[100:110, 3] = 0xFFFFFFFF
+    want = _philox_numpy(ctr, key)
+    for i in range(ctr.shape[0]):
+        assert np.array_equal(o.philox4x32_10(ctr[i].astype(np.uint32), key.astype(np.uint32)), want[i]), i
+
+
+def test_r16_past_2_35_against_numpy_restatement():
+    """Draws of elements E >= 2^35, where the high half of E/8 is counter word 3."""
+    seed, step, stream = 0xC0FFEE0012345678, 123456, 1
+    key = np.array([seed & 0xFFFFFFFF, seed >> 32], np.uint64)
+    Es = [(1 << 35) + i for i in range(40)] + [(1 << 40) + 7, (1 << 45) + 12345, (1 << 61) + 3]
+    ctr = np.array([[(E >> 3) & 0xFFFFFFFF, stream, step, E >> 35] for E in Es], np.uint64)
+    words = _philox_numpy(ctr, key)
+    for E, w in zip(Es, words):
+        word = int(w[(E >> 1) & 3])
+        want = (word >> 16) if (E & 1) else (word & 0xFFFF)
+        assert o.r16(seed, step, stream, E) == want, E
+
+
+@pytest.mark.parametrize("x", [1.0 + 2 ** -9, -0.123456, 7.77e-6, 3.0e-39])
+def test_sr_unbiased_over_philox_seeds(x):
+    """SR of a fixed x at one element, over 10^5 distinct Philox seeds: the
+    mean lies within 3 sigma of x (sigma = ulp * sqrt(p (1 - p) / n), p the
+    chance of rounding up)."""
+    n = 100_000
+    x = np.float32(x)
+    bits = int(np.array([x], np.float32).view(np.uint32)[0])
+    lo = float(_f32_from_bf16(bits >> 16))
+    hi = float(_f32_from_bf16((bits >> 16) + 1))
+    p = (float(x) - lo) / (hi - lo)
+    up = 0
+    E = 987654321
+    for seed in range(1, n + 1):
+        h = o.sr_bf16(x, o.r16(seed * 0x9E3779B97F4A7C15 & 0xFFFFFFFFFFFFFFFF, 5, 0, E))
+        assert h in (bits >> 16, (bits >> 16) + 1)
+        up += h != (bits >> 16)
+    mean = lo + (hi - lo) * up / n
+    sigma = abs(hi - lo) * np.sqrt(p * (1 - p) / n)
+    assert abs(mean - float(x)) <= 3 * sigma
