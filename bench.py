@@ -50,6 +50,9 @@ def parse():
     ap.add_argument("--optimizer", default="adamw", choices=["adamw", "momentum", "lion"],
                     help="8-bit-state optimizer of the step (adamw is the headline)")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the BF16-state, Momentum and Lion timings that follow the headline")
+    ap.add_argument("--secondary-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--cpu-blocks", type=int, default=24000,
@@ -381,6 +384,13 @@ def main():
                 "algorithmic_bytes_per_launch": abytes / nl, "peak_source": peak_kind,
                 "median_ms_per_step": statistics.median(per), "min_ms_per_step": min(per)}
 
+    # the other steps of the path, timed the same way in the same run: the
+    # BF16-state step on its GPT-Neo 2.7B list, 8-bit Momentum and Lion on the
+    # headline's 6.7B list (their one state is the headline's m codes)
+    secondary = None
+    if not args.no_secondary and not args.flat and args.workload == "gptneo-6.7b" and args.optimizer == "adamw":
+        secondary = run_secondary(args, wl, states, peak, device, world, barrier)
+
     # end to end through the public API: grads in from pinned host memory,
     # step, updated params back to pinned host memory, every step
     e2e = None
@@ -407,20 +417,94 @@ def main():
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
-            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "storage_dtype": "bf16+u8" if wl.state == "8bit" else "bf16", "data": "synthetic",
             "config": {"workload": wl.name, "optimizer": args.optimizer, "rounding": args.rounding,
                        "params": numel, "tensors": len(wl.tensors),
                        "blocks": wl.blocks(), "state": wl.state,
                        "bytes_per_step": abytes, "gbs": abytes / (ms_per_step / 1e3) / 1e9,
                        "l2": "inputs larger than L2 (%.1f GB moved per step, no flush)" % (abytes / 1e9),
                        "parallelism": "replicas x%d (each GPU steps its own full list)" % world},
-            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e,
+            "roofline": roofline, "secondary": secondary, "cpu_baseline": cpu, "e2e": e2e,
             "gpu_launches": nl * args.steps, "clocks": clock_info,
         }
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
     return 0
+
+
+def _time_steps(fn, steps, warmup, stream, device, barrier):
+    """Warm-up, then `steps` calls of fn(t) with one event pair per call on
+    the launching stream; returns the per-call milliseconds."""
+    t = 0
+    for _ in range(warmup):
+        t += 1
+        fn(t)
+    torch.cuda.synchronize(device)
+    barrier()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for k in range(steps):
+        t += 1
+        ev[k][0].record(stream)
+        fn(t)
+        ev[k][1].record(stream)
+    torch.cuda.synchronize(device)
+    barrier()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def run_secondary(args, wl8, states8, peak, device, world, barrier):
+    """BF16-state AdamW on the GPT-Neo 2.7B list, 8-bit Momentum and 8-bit
+    Lion on the 6.7B list (using the headline's parameters, gradients and m
+    state), each with the headline's warm-up and events, one launch per step.
+    Per entry: ms/step, Gparams/s, algorithmic GB/s and the fraction of the
+    measured HBM peak."""
+    import bit_blockwise_adamw_gb300 as q8
+    from bit_blockwise_adamw_gb300 import workloads as W
+    stream = torch.cuda.current_stream(device)
+    out = {}
+    h8 = dict(wl8.hp)
+
+    def entry(name, wl, kernel, moments, per, nl):
+        ms = statistics.mean(per)
+        ab = algorithmic_bytes(wl, moments)
+        gbs = ab / (ms / 1e3) / 1e9
+        out[name] = {"workload": wl.name, "kernel": kernel, "ms_per_step": ms,
+                     "median_ms_per_step": statistics.median(per), "steps": len(per),
+                     "value": world * wl.numel / (ms / 1e3) / 1e9, "unit": UNIT,
+                     "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak,
+                     "algorithmic_bytes_per_launch": ab / nl,
+                     "traffic": traffic_per_launch(kernel, wl.numel / nl) if nl == 1 else None}
+
+    # one-state steps on the 6.7B list: the m codes and absmax of the headline state
+    one = [q8.Tensor8(s.param, s.grad, m_codes=s.m_codes, m_absmax=s.m_absmax) for s in states8]
+    packed1 = q8.pack_tensor8(one)
+    nl1 = launches_per_step(wl8)
+    per = _time_steps(lambda t: q8.momentum8bit_sr_step(packed1, q8.momentum_hparams(
+        lr=h8["lr"], momentum=h8["beta1"], weight_decay=h8["weight_decay"], step=t, seed=wl8.philox_seed), stream),
+        args.secondary_steps, args.warmup, stream, device, barrier)
+    entry("momentum8bit", wl8, "step1_kernel", 1, per, nl1)
+    per = _time_steps(lambda t: q8.lion8bit_sr_step(packed1, q8.lion_hparams(
+        lr=h8["lr"] / 10, beta1=h8["beta1"], beta2=0.99, weight_decay=h8["weight_decay"], step=t,
+        seed=wl8.philox_seed), stream), args.secondary_steps, args.warmup, stream, device, barrier)
+    entry("lion8bit", wl8, "step1_kernel", 1, per, nl1)
+    del one, packed1
+
+    # the BF16-state step on its own (GPT-Neo 2.7B) list
+    wl16 = W.WORKLOADS["gptneo-2.7b-bf16"]
+    p16 = W.init_params(wl16, device)
+    g16 = W.make_grads(wl16, 1, device)
+    st16 = [q8.Tensor16(p, g, torch.zeros_like(p), torch.zeros_like(p)) for p, g in zip(p16, g16)]
+    packed16 = q8.pack_tensor16(st16)
+    h16 = dict(wl16.hp)
+    per = _time_steps(lambda t: q8.adamw_bf16_sr_step(packed16, q8.hparams(
+        lr=h16["lr"], beta1=h16["beta1"], beta2=h16["beta2"], eps=h16["eps"], weight_decay=h16["weight_decay"],
+        step=t, seed=wl16.philox_seed), stream), args.secondary_steps, args.warmup, stream, device, barrier)
+    entry("adamw_bf16", wl16, "step16_kernel", 2, per, launches_per_step(wl16))
+    del st16, packed16, p16, g16
+    torch.cuda.empty_cache()
+    return out
 
 
 def run_e2e(args, wl, states, step_fn, hp, t, device, world, barrier):

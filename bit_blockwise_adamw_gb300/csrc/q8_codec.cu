@@ -124,16 +124,14 @@ cudaError_t launch_quantize(const float* x, uint8_t* codes, float* absmax, int64
 {
     const int64_t nb = (n + kBlock - 1) / kBlock;
     if (nb == 0) return cudaSuccess;
-    static int full_s = 0, full_u = 0;
-    if (kind == Q8_SIGNED) {
-        if (full_s == 0) full_s = resident_ctas(reinterpret_cast<const void*>(quantize_kernel<Q8_SIGNED>), kThreads, 0);
-        const int grid = static_cast<int>(nb < full_s ? nb : full_s);
-        quantize_kernel<Q8_SIGNED><<<grid, kThreads, 0, st>>>(x, codes, absmax, n, nb, tab);
-    } else {
-        if (full_u == 0) full_u = resident_ctas(reinterpret_cast<const void*>(quantize_kernel<Q8_UNSIGNED>), kThreads, 0);
-        const int grid = static_cast<int>(nb < full_u ? nb : full_u);
-        quantize_kernel<Q8_UNSIGNED><<<grid, kThreads, 0, st>>>(x, codes, absmax, n, nb, tab);
-    }
+    const void* k = kind == Q8_SIGNED ? reinterpret_cast<const void*>(quantize_kernel<Q8_SIGNED>)
+                                      : reinterpret_cast<const void*>(quantize_kernel<Q8_UNSIGNED>);
+    int full = 0;
+    const cudaError_t e = persistent_grid(k, kThreads, 0, &full);
+    if (e != cudaSuccess) return e;
+    const int grid = static_cast<int>(nb < full ? nb : full);
+    if (kind == Q8_SIGNED) quantize_kernel<Q8_SIGNED><<<grid, kThreads, 0, st>>>(x, codes, absmax, n, nb, tab);
+    else quantize_kernel<Q8_UNSIGNED><<<grid, kThreads, 0, st>>>(x, codes, absmax, n, nb, tab);
     return cudaGetLastError();
 }
 
@@ -141,8 +139,9 @@ cudaError_t launch_dequantize(const uint8_t* codes, const float* absmax, float* 
                               int kind, const DevTables* tab, cudaStream_t st)
 {
     if (n == 0) return cudaSuccess;
-    static int full = 0;
-    if (full == 0) full = resident_ctas(reinterpret_cast<const void*>(dequantize_kernel), kThreads, 0);
+    int full = 0;
+    const cudaError_t e = persistent_grid(reinterpret_cast<const void*>(dequantize_kernel), kThreads, 0, &full);
+    if (e != cudaSuccess) return e;
     const int64_t groups = (n + kVec - 1) / kVec;
     const int64_t want = (groups + kThreads - 1) / kThreads;
     const int grid = static_cast<int>(want < full ? want : full);
@@ -154,8 +153,9 @@ cudaError_t launch_philox_fill(const PhiloxKey& key, uint32_t stream_id, uint64_
                                uint16_t* out, cudaStream_t st)
 {
     if (n == 0) return cudaSuccess;
-    static int full = 0;
-    if (full == 0) full = resident_ctas(reinterpret_cast<const void*>(philox_fill_kernel), kThreads, 0);
+    int full = 0;
+    const cudaError_t e = persistent_grid(reinterpret_cast<const void*>(philox_fill_kernel), kThreads, 0, &full);
+    if (e != cudaSuccess) return e;
     const uint64_t groups = ((offset & 7) + static_cast<uint64_t>(n) + 7) / 8;
     const uint64_t want = (groups + kThreads - 1) / kThreads;
     const int grid = static_cast<int>(want < static_cast<uint64_t>(full) ? want : full);

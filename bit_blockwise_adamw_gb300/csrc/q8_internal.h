@@ -160,8 +160,15 @@ void build_codebook(int kind, float out[256]);
 // Device copy of the tables for the current device, set up on first use.
 cudaError_t device_tables(const DevTables** out);
 
+// Grid of a persistent kernel on the current device: SMs x resident CTAs of
+// `kernel` at `threads` threads and `smem` bytes of dynamic shared memory.
+// Worked out once per (kernel, device) under a lock (which also raises the
+// kernel's dynamic shared-memory limit to `smem` on that device) and cached,
+// so concurrent first calls from several host threads, and processes that
+// drive several devices, each get their own device's figure.
+cudaError_t persistent_grid(const void* kernel, int threads, size_t smem, int* grid);
+
 // Launchers (one per kernel; each returns cudaGetLastError()).
-int resident_ctas(const void* kernel, int threads, size_t smem);
 cudaError_t launch_step8(const Step8Args& a, cudaStream_t st);
 cudaError_t launch_step32(const Step32Args& a, cudaStream_t st);
 cudaError_t launch_step16(const Step16Args& a, cudaStream_t st);

@@ -76,8 +76,9 @@ cudaError_t launch_selftest_sqrt_div(uint64_t* counts, cudaStream_t st)
 {
     const cudaError_t e = cudaMemsetAsync(counts, 0, 6 * sizeof(uint64_t), st);
     if (e != cudaSuccess) return e;
-    const int grid = resident_ctas(reinterpret_cast<const void*>(selftest_kernel), 256, 0);
-    if (grid <= 0) return cudaErrorUnknown;
+    int grid = 0;
+    const cudaError_t eg = persistent_grid(reinterpret_cast<const void*>(selftest_kernel), 256, 0, &grid);
+    if (eg != cudaSuccess) return eg;
     selftest_kernel<<<grid, 256, 0, st>>>(reinterpret_cast<unsigned long long*>(counts));
     return cudaGetLastError();
 }

@@ -326,17 +326,16 @@ __global__ void __launch_bounds__(kSmall1) step1_32_kernel(const __grid_constant
 template <int OPT, bool SR>
 cudaError_t launch1(const Step1Args& a, bool has_partial, cudaStream_t st)
 {
-    static int full = 0;
-    if (full == 0) {
-        const void* k = reinterpret_cast<const void*>(step1_kernel<OPT, SR>);
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem1);
-        if (e != cudaSuccess) return e;
-        full = resident_ctas(k, kT1, kSmem1);
-        if (full <= 0) return cudaErrorUnknown;
-    }
+    int full = 0, unused = 0;
+    cudaError_t e = persistent_grid(reinterpret_cast<const void*>(step1_kernel<OPT, SR>), kT1, kSmem1, &full);
+    if (e != cudaSuccess) return e;
     const int grid = a.nblocks < full ? a.nblocks : full;
     if (grid > 0) step1_kernel<OPT, SR><<<grid, kT1, kSmem1, st>>>(a);
-    if (has_partial && a.nt > 0) step1_tail_kernel<OPT, SR><<<a.nt, kT1, kSmem1, st>>>(a);
+    if (has_partial && a.nt > 0) {
+        e = persistent_grid(reinterpret_cast<const void*>(step1_tail_kernel<OPT, SR>), kT1, kSmem1, &unused);
+        if (e != cudaSuccess) return e;
+        step1_tail_kernel<OPT, SR><<<a.nt, kT1, kSmem1, st>>>(a);
+    }
     return cudaGetLastError();
 }
 

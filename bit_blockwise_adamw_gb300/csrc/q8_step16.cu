@@ -146,9 +146,11 @@ __global__ void __launch_bounds__(kThreads, 4) step16_kernel(const __grid_consta
 
 cudaError_t launch_step16(const Step16Args& a, cudaStream_t st)
 {
-    static int full = 0;
-    if (full == 0) full = resident_ctas(reinterpret_cast<const void*>(step16_kernel<true>), kThreads, 0);
-    if (full <= 0) return cudaErrorUnknown;
+    const void* k = a.s.sr ? reinterpret_cast<const void*>(step16_kernel<true>)
+                           : reinterpret_cast<const void*>(step16_kernel<false>);
+    int full = 0;
+    const cudaError_t e = persistent_grid(k, kThreads, 0, &full);
+    if (e != cudaSuccess) return e;
     const int grid = a.nblocks < full ? a.nblocks : full;
     if (grid > 0) {
         if (a.s.sr) step16_kernel<true><<<grid, kThreads, 0, st>>>(a);

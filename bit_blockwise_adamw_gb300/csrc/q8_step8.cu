@@ -373,34 +373,20 @@ __global__ void __launch_bounds__(kSmallThreads) step32_kernel(const __grid_cons
 template <bool SR>
 cudaError_t launch_step8_t(const Step8Args& a, bool has_partial, cudaStream_t st)
 {
-    static int full = 0;
-    if (full == 0) {
-        const void* k = reinterpret_cast<const void*>(step8_kernel<SR>);
-        cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        e = cudaFuncSetAttribute(reinterpret_cast<const void*>(step8_tail_kernel<SR>),
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-        if (e != cudaSuccess) return e;
-        full = resident_ctas(k, kT8, kSmemBytes);
-        if (full <= 0) return cudaErrorUnknown;
-    }
+    int full = 0, unused = 0;
+    cudaError_t e = persistent_grid(reinterpret_cast<const void*>(step8_kernel<SR>), kT8, kSmemBytes, &full);
+    if (e != cudaSuccess) return e;
     const int grid = a.nblocks < full ? a.nblocks : full;
     if (grid > 0) step8_kernel<SR><<<grid, kT8, kSmemBytes, st>>>(a);
-    if (has_partial && a.nt > 0) step8_tail_kernel<SR><<<a.nt, kT8, kSmemBytes, st>>>(a);
+    if (has_partial && a.nt > 0) {
+        e = persistent_grid(reinterpret_cast<const void*>(step8_tail_kernel<SR>), kT8, kSmemBytes, &unused);
+        if (e != cudaSuccess) return e;
+        step8_tail_kernel<SR><<<a.nt, kT8, kSmemBytes, st>>>(a);
+    }
     return cudaGetLastError();
 }
 
 }  // namespace
-
-int resident_ctas(const void* kernel, int threads, size_t smem)
-{
-    int dev = 0, sms = 0, per_sm = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
-    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem) != cudaSuccess)
-        return 0;
-    return sms * (per_sm > 0 ? per_sm : 1);
-}
 
 cudaError_t launch_step8(const Step8Args& a, cudaStream_t st)
 {

@@ -12,7 +12,9 @@
 // (largest e) up gives the tables in ascending order directly.
 #include <cmath>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <tuple>
 
 #include "q8_internal.h"
 
@@ -108,7 +110,37 @@ constexpr int kMaxDevices = 64;
 std::mutex g_mutex;
 const DevTables* g_dev_ptr[kMaxDevices] = {};
 
+// persistent_grid's cache: (kernel, device, threads, smem) -> grid.
+std::mutex g_grid_mutex;
+std::map<std::tuple<const void*, int, int, size_t>, int> g_grids;
+
 }  // namespace
+
+cudaError_t persistent_grid(const void* kernel, int threads, size_t smem, int* grid)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const auto key = std::make_tuple(kernel, dev, threads, smem);
+    std::lock_guard<std::mutex> lock(g_grid_mutex);
+    const auto it = g_grids.find(key);
+    if (it != g_grids.end()) {
+        *grid = it->second;
+        return cudaSuccess;
+    }
+    if (smem > 0) {
+        err = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+        if (err != cudaSuccess) return err;
+    }
+    int sms = 0, per_sm = 0;
+    if ((err = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return err;
+    if ((err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem)) != cudaSuccess)
+        return err;
+    if (sms <= 0 || per_sm <= 0) return cudaErrorInvalidConfiguration;
+    g_grids.emplace(key, sms * per_sm);
+    *grid = sms * per_sm;
+    return cudaSuccess;
+}
 
 void build_codebook(int kind, float out[256])
 {

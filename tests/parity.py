@@ -52,6 +52,40 @@ def compare_state8(gpu, host, where=""):
                                       err_msg="v32 " + where)
 
 
+def host_slice8(state, sl):
+    """Views into a host State8 for one sharding.Slice (block-aligned slice of
+    an 8-bit tensor, or a whole small tensor), so that the oracle's in-place
+    update of the slice writes into the full host arrays."""
+    a, b = sl.start, sl.start + sl.count
+    if state.m_codes is None:
+        return o.State8(state.param, state.grad, m32=state.m32, v32=state.v32, philox_offset=sl.philox_offset)
+    b0, b1 = a // BLOCK, (b + BLOCK - 1) // BLOCK
+    opt = lambda x, lo, hi: None if x is None else x[lo:hi]
+    return o.State8(state.param[a:b], state.grad[a:b], state.m_codes[a:b], opt(state.v_codes, a, b),
+                    state.m_absmax[b0:b1], opt(state.v_absmax, b0, b1), philox_offset=sl.philox_offset)
+
+
+def compare_slice8(gpu, host, sl, where=""):
+    """Bit-exact comparison of one rank's slice (params, codes, absmax or fp32 state)."""
+    a, b = sl.start, sl.start + sl.count
+    np.testing.assert_array_equal(u16(gpu.param[a:b]), host.param[a:b], err_msg="param " + where)
+    if host.m_codes is None:
+        np.testing.assert_array_equal(gpu.m32.cpu().numpy().view(np.uint32), host.m32.view(np.uint32),
+                                      err_msg="m32 " + where)
+        if host.v32 is not None:
+            np.testing.assert_array_equal(gpu.v32.cpu().numpy().view(np.uint32), host.v32.view(np.uint32),
+                                          err_msg="v32 " + where)
+        return
+    b0, b1 = a // BLOCK, (b + BLOCK - 1) // BLOCK
+    np.testing.assert_array_equal(gpu.m_codes[a:b].cpu().numpy(), host.m_codes[a:b], err_msg="m codes " + where)
+    np.testing.assert_array_equal(gpu.m_absmax[b0:b1].cpu().numpy().view(np.uint32),
+                                  host.m_absmax[b0:b1].view(np.uint32), err_msg="m absmax " + where)
+    if host.v_codes is not None:
+        np.testing.assert_array_equal(gpu.v_codes[a:b].cpu().numpy(), host.v_codes[a:b], err_msg="v codes " + where)
+        np.testing.assert_array_equal(gpu.v_absmax[b0:b1].cpu().numpy().view(np.uint32),
+                                      host.v_absmax[b0:b1].view(np.uint32), err_msg="v absmax " + where)
+
+
 # ---------------------------------------------------------------- sampled replay
 # Each 2048-block's trajectory depends only on its own inputs, so the oracle
 # can replay any chosen blocks over all steps.  Workers are started with

@@ -8,7 +8,7 @@ import bit_blockwise_adamw_gb300 as q8
 from bit_blockwise_adamw_gb300 import workloads as W
 import oracle as o
 
-from parity import u16
+from parity import compare_slice8, host_slice8, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -98,23 +98,39 @@ def test_model_shaped_list(cuda_device, name):
 @pytest.mark.parametrize("name", ["momentum", "lion"])
 def test_sharded_step_equals_unsharded(cuda_device, name):
     """Three data-parallel ranks emulated in sequence on one GPU, each updating
-    only its block-aligned slices with global Philox offsets: the same bits as
-    the unsharded one-state step."""
+    only its block-aligned slices with global Philox offsets.  After every
+    rank's call the oracle replays that rank's slices (one-state tensor step
+    with the slice's absmax sub-array and global offset) and the rank's params,
+    codes and absmax must equal it bit for bit; the union also equals the
+    unsharded one-state step."""
     from bit_blockwise_adamw_gb300 import sharding
-    _, fn = OPTS[name]
+    opt, fn = OPTS[name]
     wl = W.custom("shard1", [2048 * 20 + 7, 300, 4096, 2048 * 9, 65536 + 24], steps=3, data_seed=95)
     params = W.init_params(wl, cuda_device)
     whole = [q8.Tensor8.zeros_like(p.clone(), None, moments=1) for p in params]
     split = [q8.Tensor8.zeros_like(p.clone(), None, moments=1) for p in params]
+    host = [o.zeros_onestate(u16(p), np.zeros(p.numel(), np.uint16)) for p in params]
+    plan = sharding.plan([p.numel() for p in params], 3)
     for step in range(1, 4):
         grads = W.make_grads(wl, step, cuda_device)
-        for a, b, g in zip(whole, split, grads):
+        for a, b, c, g in zip(whole, split, host, grads):
             a.grad = g
             b.grad = g
-        hg, _ = _hp(name, step, 1)
+            c.grad[:] = u16(g)
+        hg, hh = _hp(name, step, 1)
         fn(whole, hg)
         for rank in range(3):
             fn(sharding.shard(split, 3, rank), hg)
+            for sl in plan[rank]:
+                hs = host_slice8(host[sl.tensor], sl)
+                if hs.m_codes is not None:
+                    o.onestate8bit_tensor(opt, hs, sl.philox_offset, hh)
+                else:
+                    o.onestate32_tensor(opt, hs, sl.philox_offset, hh)
+            torch.cuda.synchronize()
+            for sl in plan[rank]:
+                compare_slice8(split[sl.tensor], host[sl.tensor], sl,
+                               "%s rank %d, tensor %d, step %d" % (name, rank, sl.tensor, step))
     torch.cuda.synchronize()
     for a, b in zip(whole, split):
         assert torch.equal(a.param, b.param)

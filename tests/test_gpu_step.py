@@ -15,7 +15,8 @@ import bit_blockwise_adamw_gb300 as q8
 from bit_blockwise_adamw_gb300 import workloads as W
 import oracle as o
 
-from parity import (SampledRun, compare_state8, gpu_states8, host_states8, hp_for, oracle_pool, u16)
+from parity import (SampledRun, compare_slice8, compare_state8, gpu_states8, host_slice8, host_states8, hp_for,
+                    oracle_pool, u16)
 
 pytestmark = pytest.mark.gpu
 
@@ -252,22 +253,39 @@ def test_tensor_beyond_2_31_elements(cuda_device, pool, state):
 @pytest.mark.parametrize("world", [2, 3, 8])
 def test_sharded_step_equals_unsharded(cuda_device, world):
     """N data-parallel ranks emulated in sequence on one GPU: each updates only
-    its block-aligned slices (global Philox offsets); the result equals the
-    unsharded step bit for bit, states included."""
+    its block-aligned slices (global Philox offsets).  After every rank's call
+    the oracle replays that rank's slices from the same inputs (its 8-bit
+    tensor step on the slice, with the slice's absmax sub-arrays and global
+    offset) and the rank's params, codes and absmax must equal it bit for bit;
+    after every step the union also equals the unsharded CUDA step."""
     from bit_blockwise_adamw_gb300 import sharding
     wl = W.custom("shard", [2048 * 50 + 7, 300, 4096, 2048 * 9, 1000, 65536 + 24], steps=3, data_seed=84)
     params = W.init_params(wl, cuda_device)
     whole = gpu_states8([p.clone() for p in params])
     split = gpu_states8([p.clone() for p in params])
+    host = host_states8([u16(p) for p in params])
+    plan = sharding.plan([p.numel() for p in params], world)
     for step in range(1, 4):
         grads = W.make_grads(wl, step, cuda_device)
-        h = q8.hparams(**hp_for(wl, step))
-        for a, b, g in zip(whole, split, grads):
+        hd = hp_for(wl, step)
+        h = q8.hparams(**hd)
+        for a, b, c, g in zip(whole, split, host, grads):
             a.grad = g
             b.grad = g
+            c.grad[:] = u16(g)
         q8.adamw8bit_sr_step(whole, h)
         for rank in range(world):
             q8.adamw8bit_sr_step(sharding.shard(split, world, rank), h)
+            for sl in plan[rank]:
+                hs = host_slice8(host[sl.tensor], sl)
+                if hs.m_codes is not None:
+                    o.adamw8bit_tensor(hs, sl.philox_offset, o.hparams(**hd))
+                else:
+                    o.adamw32_tensor(hs, sl.philox_offset, o.hparams(**hd))
+            torch.cuda.synchronize()
+            for sl in plan[rank]:
+                compare_slice8(split[sl.tensor], host[sl.tensor], sl,
+                               "rank %d of %d, tensor %d, step %d" % (rank, world, sl.tensor, step))
     torch.cuda.synchronize()
     for a, b in zip(whole, split):
         assert torch.equal(a.param, b.param)
