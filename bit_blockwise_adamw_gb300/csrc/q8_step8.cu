@@ -5,17 +5,21 @@
 // written with stochastic rounding), and its fp32-state path for tensors below
 // 4096 elements (same page, scoping comment).
 //
-// Layout: a persistent grid of resident CTAs (a multiple of the SM count);
-// each CTA stages the codebooks and the cell search tables in shared memory
-// once, then walks a contiguous range of 2048-element blocks.  The partial
-// last block of a tensor (if its length is not a multiple of 2048) goes to a
-// small second kernel, so the hot loop has only full-block code.  Per block each
-// of its 128 threads owns sixteen contiguous elements: 16-byte streaming
-// loads of grad, param and both code arrays.  The kernel is bound by
-// instruction issue rather than by DRAM, so the loop is written to keep the
-// instruction count down: packed fp32x2 arithmetic (with a packed exact square
-// root and division wherever a thread's values allow it), one shared-memory
-// lookup per code, warp reductions with redux.sync.
+// Layout: one persistent CTA per SM, made of seven independent groups of 128
+// threads.  The CTA stages the search tables and a lane-replicated copy of the
+// two codebooks in shared memory once (one copy per SM serves all seven
+// groups); each group then walks its own contiguous range of 2048-element
+// blocks, synchronising only with itself (a named barrier per group).  The
+// partial last block of a tensor (if its length is not a multiple of 2048)
+// goes to a small second kernel, so the hot loop has only full-block code.
+// Per block each of a group's 128 threads owns sixteen contiguous elements:
+// 16-byte streaming loads of grad, param and both code arrays.  The kernel is
+// bound by instruction issue rather than by DRAM, so the loop is written to
+// keep the instruction count down: packed fp32x2 arithmetic (with a packed
+// exact square root and division wherever a thread's values allow it),
+// codebook lookups whose address is one byte permute and that never share a
+// shared-memory bank within a warp, one lookup per code in the search, warp
+// reductions with redux.sync.
 #include "q8_device.cuh"
 
 namespace q8 {
@@ -32,15 +36,26 @@ __device__ __forceinline__ int find_tensor(const int32_t* start, int nt, int gb)
     return lo;
 }
 
-// Each CTA of 128 threads owns one 2048-element block per iteration, sixteen
-// contiguous elements per thread: per-block work (tensor lookup, absmax
-// reduction, reciprocals) is spread over twice as many elements as with
-// eight, and every code load is a full 16-byte vector.
+// Each group of 128 threads owns one 2048-element block per iteration,
+// sixteen contiguous elements per thread: per-block work (tensor lookup,
+// absmax reduction, reciprocals) is spread over twice as many elements as
+// with eight, and every code load is a full 16-byte vector.  Seven groups per
+// CTA (72 registers a thread); six or eight measured slower.
 constexpr int kT8 = 128;
 constexpr int kV8 = 16;
 constexpr int kW8 = kT8 / 32;
-static_assert(kT8 * kV8 == kBlock, "one block per CTA iteration");
-constexpr int kSmemBytes = static_cast<int>(sizeof(DevTables)) + 2 * kW8 * 8;
+constexpr int kGroups = 7;
+static_assert(kT8 * kV8 == kBlock, "one block per group iteration");
+
+// Codebooks replicated per lane: row i (256 bytes) holds Cs[i] for lanes
+// 0..31, then Cu[i] for lanes 0..31.  Lane l reads word l of the half-row,
+// so the 32 lookups of a warp fall in 32 different banks whatever the codes,
+// and the byte offset (code << 8) | (4 * lane) is a single byte permute.
+constexpr int kLutBytes = 256 * 256;
+constexpr int kRedBytes = 2 * kW8 * 8;                       // per group
+constexpr int kSmemBytes = kLutBytes + static_cast<int>(sizeof(DevTables)) + kGroups * kRedBytes;
+constexpr int kTailSmemBytes = static_cast<int>(sizeof(DevTables)) + kRedBytes;
+static_assert(kSmemBytes <= 227 * 1024, "shared memory of one CTA");
 
 struct Frag {                  // one thread's sixteen elements of one block
     uint32_t g[8], p[8], mc[4], vc[4];
@@ -116,8 +131,9 @@ __device__ __forceinline__ float absmin4(float2 a, float2 b)
     return fminf(min3(fabsf(a.x), fabsf(a.y), fabsf(b.x)), fabsf(b.y));
 }
 
-// Shared-memory view of the staged tables and the reduction scratch.
+// Shared-memory view of the staged tables and of a group's reduction scratch.
 struct Smem8 {
+    uint32_t lut;              // shared address of the lane-replicated codebooks (main kernel)
     const float* cs;
     const float* cu;
     const uint32_t* cell_s;
@@ -125,14 +141,51 @@ struct Smem8 {
     uint2* red;                // [2][kW8]
 };
 
-__device__ __forceinline__ Smem8 stage_tables(const DevTables* tab, unsigned char* smem)
+// Copy the tables to shared memory at `smem` (all `nthreads` threads of the
+// CTA take part, then a CTA barrier).
+__device__ __forceinline__ const DevTables* copy_tables(const DevTables* tab, unsigned char* smem, int nthreads)
 {
     const uint4* src = reinterpret_cast<const uint4*>(tab);
     uint4* dst = reinterpret_cast<uint4*>(smem);
-    for (int i = threadIdx.x; i < static_cast<int>(sizeof(DevTables) / 16); i += kT8) dst[i] = src[i];
+    for (int i = threadIdx.x; i < static_cast<int>(sizeof(DevTables) / 16); i += nthreads) dst[i] = src[i];
+    return reinterpret_cast<const DevTables*>(smem);
+}
+
+// The main kernel's shared memory: the lane-replicated codebooks, the tables,
+// then one reduction scratch per group.
+__device__ __forceinline__ Smem8 stage_main(const DevTables* tab, unsigned char* smem, int grp)
+{
+    float* lut = reinterpret_cast<float*>(smem);
+    for (int i = threadIdx.x; i < kLutBytes / 4; i += kGroups * kT8) {
+        const int row = i >> 6, col = i & 63;
+        lut[i] = col < 32 ? tab->cs[row] : tab->cu[row];
+    }
+    const DevTables* t = copy_tables(tab, smem + kLutBytes, kGroups * kT8);
     __syncthreads();
-    const DevTables* t = reinterpret_cast<const DevTables*>(smem);
-    return Smem8{t->cs, t->cu, t->cell_s, t->cell_u, reinterpret_cast<uint2*>(smem + sizeof(DevTables))};
+    uint2* red = reinterpret_cast<uint2*>(smem + kLutBytes + sizeof(DevTables) + grp * kRedBytes);
+    return Smem8{static_cast<uint32_t>(__cvta_generic_to_shared(smem)), t->cs, t->cu, t->cell_s, t->cell_u, red};
+}
+
+// The tail kernel's: the tables and one reduction scratch.
+__device__ __forceinline__ Smem8 stage_tail(const DevTables* tab, unsigned char* smem)
+{
+    const DevTables* t = copy_tables(tab, smem, kT8);
+    __syncthreads();
+    return Smem8{0u, t->cs, t->cu, t->cell_s, t->cell_u, reinterpret_cast<uint2*>(smem + sizeof(DevTables))};
+}
+
+__device__ __forceinline__ float lds_f32(uint32_t addr)
+{
+    float v;
+    asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+// Barrier of one group's 128 threads (id 0 is the whole-CTA barrier, which a
+// 128-thread CTA also uses this way).
+__device__ __forceinline__ void bar_group(int id)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kT8) : "memory");
 }
 
 // The L2 prefetch thread 0 issues during a block: the inputs of global block
@@ -143,15 +196,15 @@ struct Prefetch {
     bool on;
 };
 
-// One 2048-element block of one tensor.  FULL: every thread owns sixteen
-// valid elements (the hot path: vector loads and stores only); otherwise the
-// block is the partial last block of its tensor.  `it` picks the half of the
-// double-buffered reduction scratch.
+// One 2048-element block of one tensor, by one group (`tid` = thread of the
+// group, `bar` = the group's barrier id).  FULL: every thread owns sixteen
+// valid elements (the hot path: vector loads and stores only, lane-replicated
+// codebooks); otherwise the block is the partial last block of its tensor.
+// `it` picks the half of the double-buffered reduction scratch.
 template <bool SR, bool FULL>
 __device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int lb, int it, const Smem8& sm,
-                                           const Prefetch& pf)
+                                           const Prefetch& pf, int tid, int bar)
 {
-    const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int64_t i0 = static_cast<int64_t>(lb) * kBlock + tid * kV8;
@@ -173,7 +226,7 @@ __device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int
         f.vc[0] = vq.x; f.vc[1] = vq.y; f.vc[2] = vq.z; f.vc[3] = vq.w;
         // after this block's own loads are in flight, so that the prefetch's
         // work hides in their latency instead of delaying them
-        if (threadIdx.x == 0 && pf.on) {
+        if (tid == 0 && pf.on) {
             if (pf.target < pf.next) {
                 prefetch_block(d, pf.target - pf.base);
             } else {
@@ -195,12 +248,23 @@ __device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int
         draws8(E, 0u, s.key, r);
         draws8(E + 8, 0u, s.key, r + 4);
     }
+    const uint32_t lw = static_cast<uint32_t>(lane) * 4u;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const uint32_t cw = f.mc[k >> 1], vw = f.vc[k >> 1];
-        const int b0 = (k & 1) * 2;
-        m[k] = __fmul2_rn(make_float2(sm.cs[byte_of(cw, b0)], sm.cs[byte_of(cw, b0 + 1)]), Mold);
-        v[k] = __fmul2_rn(make_float2(sm.cu[byte_of(vw, b0)], sm.cu[byte_of(vw, b0 + 1)]), Vold);
+        const uint32_t b0 = (k & 1) * 2;
+        if constexpr (FULL) {
+            // byte offset (code << 8) | (4 * lane): byte b of the code word
+            // into byte 1, byte 0 of lw into byte 0, zeros above
+            const uint32_t sm0 = 0x5504u | (b0 << 4), sm1 = 0x5504u | ((b0 + 1) << 4);
+            m[k] = __fmul2_rn(make_float2(lds_f32(sm.lut + __byte_perm(cw, lw, sm0)),
+                                          lds_f32(sm.lut + __byte_perm(cw, lw, sm1))), Mold);
+            v[k] = __fmul2_rn(make_float2(lds_f32(sm.lut + 128u + __byte_perm(vw, lw, sm0)),
+                                          lds_f32(sm.lut + 128u + __byte_perm(vw, lw, sm1))), Vold);
+        } else {
+            m[k] = __fmul2_rn(make_float2(sm.cs[byte_of(cw, b0)], sm.cs[byte_of(cw, b0 + 1)]), Mold);
+            v[k] = __fmul2_rn(make_float2(sm.cu[byte_of(vw, b0)], sm.cu[byte_of(vw, b0 + 1)]), Vold);
+        }
         moments2(s, bf16x2(f.g[k]), m[k], v[k]);
     }
     if constexpr (!FULL) {
@@ -246,7 +310,7 @@ __device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int
     const uint32_t wv = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(lv));
     uint2* red = sm.red + (it & 1) * kW8;                // double-buffered: one barrier per block
     if (lane == 0) red[warp] = make_uint2(wm, wv);
-    __syncthreads();
+    bar_group(bar);
     const uint2 t = lane < kW8 ? red[lane] : make_uint2(0u, 0u);
     const float M = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, t.x));
     const float V = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, t.y));
@@ -287,21 +351,25 @@ __device__ __forceinline__ bool is_partial(const Desc8& d, int lb)
 
 // The hot kernel: every full block of the launch's list.  Partial last blocks
 // are left to step8_tail_kernel, so this loop carries no ragged-tail code.
-// Each CTA takes a contiguous range of the list's blocks (end to end over the
-// tensors).
+// Each group of each CTA takes a contiguous range of the list's blocks (end to
+// end over the tensors).
 template <bool SR>
-__global__ void __launch_bounds__(kT8, 7) step8_kernel(const __grid_constant__ Step8Args a)
+__global__ void __launch_bounds__(kT8 * kGroups, 1) step8_kernel(const __grid_constant__ Step8Args a)
 {
     extern __shared__ __align__(16) unsigned char smem[];
-    const Smem8 sm = stage_tables(a.tab, smem);
+    const int grp = threadIdx.x / kT8;
+    const int tid = threadIdx.x % kT8;
+    const Smem8 sm = stage_main(a.tab, smem, grp);
+    const int worker = blockIdx.x * kGroups + grp;
+    const int nworkers = gridDim.x * kGroups;
 
-    const int begin = static_cast<int>((static_cast<int64_t>(blockIdx.x) * a.nblocks) / gridDim.x);
-    const int end = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * a.nblocks) / gridDim.x);
+    const int begin = static_cast<int>((static_cast<int64_t>(worker) * a.nblocks) / nworkers);
+    const int end = static_cast<int>((static_cast<int64_t>(worker + 1) * a.nblocks) / nworkers);
     int ti = begin < end ? find_tensor(a.blk_start, a.nt, begin) : 0;
-    // L2 prefetch: thread 0 keeps the inputs of the block two ahead in flight
-    // (one, three, four or six ahead, or none, measured slower)
+    // L2 prefetch: thread 0 of the group keeps the inputs of the block two
+    // ahead in flight (one or none measured slower, three the same)
     constexpr int kAhead = 2;
-    if (threadIdx.x == 0) {
+    if (tid == 0) {
         int tq = ti;
         for (int pg = begin; pg < end && pg < begin + kAhead; ++pg) {
             while (pg >= a.blk_start[tq + 1]) ++tq;
@@ -317,7 +385,8 @@ __global__ void __launch_bounds__(kT8, 7) step8_kernel(const __grid_constant__ S
         const int next = a.blk_start[ti + 1];
         const int full_end = min(min(end, next), base + static_cast<int>(d.n / kBlock));
         for (; gb < full_end; ++gb)
-            block_step<SR, true>(a.s, d, gb - base, it++, sm, Prefetch{&a, gb + kAhead, next, base, ti, gb + kAhead < end});
+            block_step<SR, true>(a.s, d, gb - base, it++, sm, Prefetch{&a, gb + kAhead, next, base, ti, gb + kAhead < end},
+                                 tid, 1 + grp);
         gb = min(end, next);                             // a partial last block is the tail kernel's
     }
 }
@@ -331,8 +400,8 @@ __global__ void __launch_bounds__(kT8) step8_tail_kernel(const __grid_constant__
     const int lb = static_cast<int>((d.n - 1) / kBlock);
     if (!is_partial(d, lb)) return;
     extern __shared__ __align__(16) unsigned char smem[];
-    const Smem8 sm = stage_tables(a.tab, smem);
-    block_step<SR, false>(a.s, d, lb, 0, sm, Prefetch{&a, 0, 0, 0, 0, false});
+    const Smem8 sm = stage_tail(a.tab, smem);
+    block_step<SR, false>(a.s, d, lb, 0, sm, Prefetch{&a, 0, 0, 0, 0, false}, static_cast<int>(threadIdx.x), 0);
 }
 
 // fp32-state path: one CTA per tensor (numel < 4096 = 512 threads x 8).
@@ -374,14 +443,15 @@ template <bool SR>
 cudaError_t launch_step8_t(const Step8Args& a, bool has_partial, cudaStream_t st)
 {
     int full = 0, unused = 0;
-    cudaError_t e = persistent_grid(reinterpret_cast<const void*>(step8_kernel<SR>), kT8, kSmemBytes, &full);
+    cudaError_t e = persistent_grid(reinterpret_cast<const void*>(step8_kernel<SR>), kT8 * kGroups, kSmemBytes, &full);
     if (e != cudaSuccess) return e;
-    const int grid = a.nblocks < full ? a.nblocks : full;
-    if (grid > 0) step8_kernel<SR><<<grid, kT8, kSmemBytes, st>>>(a);
+    const int per = (a.nblocks + kGroups - 1) / kGroups;     // CTAs that have blocks for every group
+    const int grid = per < full ? per : full;
+    if (grid > 0) step8_kernel<SR><<<grid, kT8 * kGroups, kSmemBytes, st>>>(a);
     if (has_partial && a.nt > 0) {
-        e = persistent_grid(reinterpret_cast<const void*>(step8_tail_kernel<SR>), kT8, kSmemBytes, &unused);
+        e = persistent_grid(reinterpret_cast<const void*>(step8_tail_kernel<SR>), kT8, kTailSmemBytes, &unused);
         if (e != cudaSuccess) return e;
-        step8_tail_kernel<SR><<<a.nt, kT8, kSmemBytes, st>>>(a);
+        step8_tail_kernel<SR><<<a.nt, kT8, kTailSmemBytes, st>>>(a);
     }
     return cudaGetLastError();
 }
