@@ -197,13 +197,14 @@ struct Prefetch {
 };
 
 // One 2048-element block of one tensor, by one group (`tid` = thread of the
-// group, `bar` = the group's barrier id).  FULL: every thread owns sixteen
+// group, `bar` = the group's barrier id, `lead` = the thread that issues the
+// L2 prefetch and stores the block absmax).  FULL: every thread owns sixteen
 // valid elements (the hot path: vector loads and stores only, lane-replicated
 // codebooks); otherwise the block is the partial last block of its tensor.
 // `it` picks the half of the double-buffered reduction scratch.
 template <bool SR, bool FULL>
 __device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int lb, int it, const Smem8& sm,
-                                           const Prefetch& pf, int tid, int bar)
+                                           const Prefetch& pf, int tid, int bar, int lead)
 {
     const int lane = tid & 31;
     const int warp = tid >> 5;
@@ -226,7 +227,7 @@ __device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int
         f.vc[0] = vq.x; f.vc[1] = vq.y; f.vc[2] = vq.z; f.vc[3] = vq.w;
         // after this block's own loads are in flight, so that the prefetch's
         // work hides in their latency instead of delaying them
-        if (tid == 0 && pf.on) {
+        if (tid == lead && pf.on) {
             if (pf.target < pf.next) {
                 prefetch_block(d, pf.target - pf.base);
             } else {
@@ -338,7 +339,7 @@ __device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int
     } else if (rem > 0) {
         store_ragged(d, i0, rem, po, mo, vo);
     }
-    if (tid == 0) {
+    if (tid == lead) {
         d.ma[lb] = M;
         d.va[lb] = V;
     }
@@ -366,10 +367,16 @@ __global__ void __launch_bounds__(kT8 * kGroups, 1) step8_kernel(const __grid_co
     const int begin = static_cast<int>((static_cast<int64_t>(worker) * a.nblocks) / nworkers);
     const int end = static_cast<int>((static_cast<int64_t>(worker + 1) * a.nblocks) / nworkers);
     int ti = begin < end ? find_tensor(a.blk_start, a.nt, begin) : 0;
-    // L2 prefetch: thread 0 of the group keeps the inputs of the block two
-    // ahead in flight (one or none measured slower, three the same)
+    // The leader thread of the group does the group's single-thread work: the
+    // L2 prefetch (the inputs of the block two ahead, kept in flight; one or
+    // none measured slower, three the same) and the block absmax stores.  The
+    // CTA's warp w runs on sub-partition w % 4 of the SM, so the leaders of
+    // the seven groups sit in warps of different sub-partitions; with all of
+    // them in each group's first warp, one sub-partition carried the extra
+    // work and the others waited for it at the group barriers (3.4 % slower).
+    const int lead = (grp & 3) * 32;
     constexpr int kAhead = 2;
-    if (tid == 0) {
+    if (tid == lead) {
         int tq = ti;
         for (int pg = begin; pg < end && pg < begin + kAhead; ++pg) {
             while (pg >= a.blk_start[tq + 1]) ++tq;
@@ -386,7 +393,7 @@ __global__ void __launch_bounds__(kT8 * kGroups, 1) step8_kernel(const __grid_co
         const int full_end = min(min(end, next), base + static_cast<int>(d.n / kBlock));
         for (; gb < full_end; ++gb)
             block_step<SR, true>(a.s, d, gb - base, it++, sm, Prefetch{&a, gb + kAhead, next, base, ti, gb + kAhead < end},
-                                 tid, 1 + grp);
+                                 tid, 1 + grp, lead);
         gb = min(end, next);                             // a partial last block is the tail kernel's
     }
 }
@@ -401,7 +408,7 @@ __global__ void __launch_bounds__(kT8) step8_tail_kernel(const __grid_constant__
     if (!is_partial(d, lb)) return;
     extern __shared__ __align__(16) unsigned char smem[];
     const Smem8 sm = stage_tail(a.tab, smem);
-    block_step<SR, false>(a.s, d, lb, 0, sm, Prefetch{&a, 0, 0, 0, 0, false}, static_cast<int>(threadIdx.x), 0);
+    block_step<SR, false>(a.s, d, lb, 0, sm, Prefetch{&a, 0, 0, 0, 0, false}, static_cast<int>(threadIdx.x), 0, 0);
 }
 
 // fp32-state path: one CTA per tensor (numel < 4096 = 512 threads x 8).
