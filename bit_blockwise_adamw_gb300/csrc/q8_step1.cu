@@ -5,10 +5,12 @@
 // to the gradient) and Lion ("Stochastic rounding support for 8-bit
 // optimizers", motivation: 8-bit Lion; Chen et al. 2023, decoupled decay).
 //
-// Same layout as the fused AdamW step: a persistent grid of 128-thread CTAs,
-// one 2048-element block per iteration, sixteen elements per thread, the
-// signed codebook and its cell table in shared memory, partial last blocks in
-// a tail kernel, tensors below 4096 elements on an fp32-state kernel.
+// Same layout as the fused AdamW step: one persistent CTA per SM made of
+// seven independent groups of 128 threads, one 2048-element block per group
+// iteration, sixteen elements per thread, the signed cell table and a
+// lane-replicated signed codebook in shared memory (one copy per SM), the
+// group leaders spread over the SM's sub-partitions, partial last blocks in a
+// tail kernel, tensors below 4096 elements on an fp32-state kernel.
 // Traffic: 8 bytes per parameter plus 8 per block (grad 2, param 2+2, code 1+1).
 #include "q8_device.cuh"
 
@@ -26,7 +28,16 @@ struct Tables1 {               // the part of DevTables this kernel stages
     uint32_t cell_s[kCellSEntries];
 };
 static_assert(sizeof(Tables1) % 16 == 0, "staged 16 bytes at a time");
-constexpr int kSmem1 = static_cast<int>(sizeof(Tables1)) + 2 * kW1 * 4;
+constexpr int kGroups1 = 7;                    // 72 registers a thread; eight groups spill
+// Lane-replicated signed codebook: row c (256 bytes) holds Cs[c] for lanes
+// 0..31 in its first 128 bytes, so lane l's lookup reads word l of the row
+// (no two lanes of a warp share a bank) at byte offset (c << 8) | (4 * l),
+// one byte permute of the code word.  The rows keep the AdamW kernel's
+// 256-byte stride so that the same permute forms the address.
+constexpr int kLut1 = 256 * 256;
+constexpr int kRed1 = 2 * kW1 * 4;
+constexpr int kSmem1 = static_cast<int>(sizeof(Tables1)) + kRed1;
+constexpr int kSmem1Main = kLut1 + static_cast<int>(sizeof(Tables1)) + kGroups1 * kRed1;
 
 // Prefetch the inputs of local block `lb` (grad, param, codes), clipped to
 // whole 16-byte chunks inside the tensor.
@@ -53,15 +64,28 @@ __device__ __forceinline__ int find_tensor1(const int32_t* start, int nt, int gb
     return lo;
 }
 
-__device__ __forceinline__ const Tables1* stage1(const DevTables* tab, unsigned char* smem)
+__device__ __forceinline__ const Tables1* stage1(const DevTables* tab, unsigned char* smem, int nthreads = kT1)
 {
     Tables1* t = reinterpret_cast<Tables1*>(smem);
-    for (int i = threadIdx.x; i < 256; i += kT1) t->cs[i] = tab->cs[i];
+    for (int i = threadIdx.x; i < 256; i += nthreads) t->cs[i] = tab->cs[i];
     const uint4* src = reinterpret_cast<const uint4*>(tab->cell_s);
     uint4* dst = reinterpret_cast<uint4*>(t->cell_s);
-    for (int i = threadIdx.x; i < kCellSEntries / 4; i += kT1) dst[i] = src[i];
+    for (int i = threadIdx.x; i < kCellSEntries / 4; i += nthreads) dst[i] = src[i];
     __syncthreads();
     return t;
+}
+
+__device__ __forceinline__ float lds_f32_1(uint32_t addr)
+{
+    float v;
+    asm("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(addr));
+    return v;
+}
+
+// Barrier of one group's 128 threads (id 0: the 128-thread tail CTA).
+__device__ __forceinline__ void bar_group1(int id)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kT1) : "memory");
 }
 
 // sign(c) as a float: +-1 with the sign bit of c, and +0 for +-0 and NaN
@@ -126,7 +150,10 @@ __device__ __forceinline__ float onestate(const Scalars1& s, float g, float p, f
     }
 }
 
-// One block; FULL = sixteen valid elements per thread.
+// One block, by one group (`tid` = thread of the group, `bar` = its barrier
+// id, `lead` = the thread that issues the L2 prefetch and stores the absmax,
+// `lut` = shared address of the lane-replicated codebook); FULL = sixteen
+// valid elements per thread.
 // The L2 prefetch thread 0 issues during a block: the inputs of global block
 // `target` (when `on`), which lies in the current tensor if target < next.
 struct Prefetch1 {
@@ -137,9 +164,8 @@ struct Prefetch1 {
 
 template <int OPT, bool SR, bool FULL>
 __device__ __forceinline__ void block1(const Scalars1& s, const Desc8& d, int lb, int it, const Tables1* tb,
-                                       uint32_t* red2, const Prefetch1& pf)
+                                       uint32_t* red2, const Prefetch1& pf, int tid, int bar, int lead, uint32_t lut)
 {
-    const int tid = threadIdx.x;
     const int lane = tid & 31;
     const int warp = tid >> 5;
     const int64_t i0 = static_cast<int64_t>(lb) * kBlock + tid * kV1;
@@ -155,7 +181,7 @@ __device__ __forceinline__ void block1(const Scalars1& s, const Desc8& d, int lb
         pw[0] = p0.x; pw[1] = p0.y; pw[2] = p0.z; pw[3] = p0.w; pw[4] = p1.x; pw[5] = p1.y; pw[6] = p1.z; pw[7] = p1.w;
         mc[0] = mq.x; mc[1] = mq.y; mc[2] = mq.z; mc[3] = mq.w;
         // after this block's own loads are in flight
-        if (threadIdx.x == 0 && pf.on) {
+        if (tid == lead && pf.on) {
             if (pf.target < pf.next) {
                 prefetch_block1(d, pf.target - pf.base);
             } else {
@@ -188,11 +214,16 @@ __device__ __forceinline__ void block1(const Scalars1& s, const Desc8& d, int lb
         draws8(E, 0u, s.key, r);
         draws8(E + 8, 0u, s.key, r + 4);
     }
+    const uint32_t lw = static_cast<uint32_t>(lane) * 4u;
 #pragma unroll
     for (int k = 0; k < 8; ++k) {
         const uint32_t cw = mc[k >> 1];
-        const int b0 = (k & 1) * 2;
-        m[k] = __fmul2_rn(make_float2(tb->cs[byte_of(cw, b0)], tb->cs[byte_of(cw, b0 + 1)]), Mold);
+        const uint32_t b0 = (k & 1) * 2;
+        if constexpr (FULL)
+            m[k] = __fmul2_rn(make_float2(lds_f32_1(lut + __byte_perm(cw, lw, 0x5504u | (b0 << 4))),
+                                          lds_f32_1(lut + __byte_perm(cw, lw, 0x5504u | ((b0 + 1) << 4)))), Mold);
+        else
+            m[k] = __fmul2_rn(make_float2(tb->cs[byte_of(cw, b0)], tb->cs[byte_of(cw, b0 + 1)]), Mold);
         po[k] = round2<SR>(onestate2<OPT>(s, bf16x2(gw[k]), bf16x2(pw[k]), m[k]), r[k]);
     }
     if constexpr (FULL) {
@@ -212,7 +243,7 @@ __device__ __forceinline__ void block1(const Scalars1& s, const Desc8& d, int lb
     const uint32_t wm = __reduce_max_sync(0xFFFFFFFFu, __float_as_uint(lm));
     uint32_t* red = red2 + (it & 1) * kW1;
     if (lane == 0) red[warp] = wm;
-    __syncthreads();
+    bar_group1(bar);
     const float M = __uint_as_float(__reduce_max_sync(0xFFFFFFFFu, lane < kW1 ? red[lane] : 0u));
 
     // absmax 0 needs no branch: m * RN(1/0) saturates to +0, the zero code 127
@@ -236,7 +267,7 @@ __device__ __forceinline__ void block1(const Scalars1& s, const Desc8& d, int lb
             }
         }
     }
-    if (tid == 0) d.ma[lb] = M;
+    if (tid == lead) d.ma[lb] = M;
 }
 
 __device__ __forceinline__ bool partial1(const Desc8& d, int lb)
@@ -245,18 +276,32 @@ __device__ __forceinline__ bool partial1(const Desc8& d, int lb)
 }
 
 template <int OPT, bool SR>
-__global__ void __launch_bounds__(kT1, 8) step1_kernel(const __grid_constant__ Step1Args a)
+__global__ void __launch_bounds__(kT1 * kGroups1, 1) step1_kernel(const __grid_constant__ Step1Args a)
 {
     extern __shared__ __align__(16) unsigned char smem[];
-    const Tables1* tb = stage1(a.tab, smem);
-    uint32_t* red = reinterpret_cast<uint32_t*>(smem + sizeof(Tables1));
-    const int begin = static_cast<int>((static_cast<int64_t>(blockIdx.x) * a.nblocks) / gridDim.x);
-    const int end = static_cast<int>((static_cast<int64_t>(blockIdx.x + 1) * a.nblocks) / gridDim.x);
+    const int grp = threadIdx.x / kT1;
+    const int tid = threadIdx.x % kT1;
+    {   // the lane-replicated codebook, then the tables
+        float* lut = reinterpret_cast<float*>(smem);
+        for (int i = threadIdx.x; i < kLut1 / 4; i += kT1 * kGroups1) {
+            const int row = i >> 6, col = i & 63;
+            lut[i] = col < 32 ? a.tab->cs[row] : 0.0f;
+        }
+    }
+    const Tables1* tb = stage1(a.tab, smem + kLut1, kT1 * kGroups1);
+    const uint32_t lut = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+    uint32_t* red = reinterpret_cast<uint32_t*>(smem + kLut1 + sizeof(Tables1) + grp * kRed1);
+    // the groups' single-thread work in warps of different SM sub-partitions
+    // (warp w of the CTA runs on sub-partition w % 4)
+    const int lead = (grp & 3) * 32;
+    const int worker = blockIdx.x * kGroups1 + grp;
+    const int nworkers = gridDim.x * kGroups1;
+    const int begin = static_cast<int>((static_cast<int64_t>(worker) * a.nblocks) / nworkers);
+    const int end = static_cast<int>((static_cast<int64_t>(worker + 1) * a.nblocks) / nworkers);
     int ti = begin < end ? find_tensor1(a.blk_start, a.nt, begin) : 0;
-    // L2 prefetch: thread 0 keeps the inputs of the next block in flight (two
-    // ahead measured slower)
+    // L2 prefetch: the leader keeps the inputs of the next block in flight
     constexpr int kAhead = 1;
-    if (threadIdx.x == 0) {
+    if (tid == lead) {
         int tq = ti;
         for (int pg = begin; pg < end && pg < begin + kAhead; ++pg) {
             while (pg >= a.blk_start[tq + 1]) ++tq;
@@ -272,7 +317,8 @@ __global__ void __launch_bounds__(kT1, 8) step1_kernel(const __grid_constant__ S
         const int next = a.blk_start[ti + 1];
         const int full_end = min(min(end, next), base + static_cast<int>(d.n / kBlock));
         for (; gb < full_end; ++gb)
-            block1<OPT, SR, true>(a.s, d, gb - base, it++, tb, red, Prefetch1{&a, gb + kAhead, next, base, ti, gb + kAhead < end});
+            block1<OPT, SR, true>(a.s, d, gb - base, it++, tb, red, Prefetch1{&a, gb + kAhead, next, base, ti, gb + kAhead < end},
+                                  tid, 1 + grp, lead, lut);
         gb = min(end, next);
     }
 }
@@ -286,7 +332,7 @@ __global__ void __launch_bounds__(kT1) step1_tail_kernel(const __grid_constant__
     extern __shared__ __align__(16) unsigned char smem[];
     const Tables1* tb = stage1(a.tab, smem);
     uint32_t* red = reinterpret_cast<uint32_t*>(smem + sizeof(Tables1));
-    block1<OPT, SR, false>(a.s, d, lb, 0, tb, red, Prefetch1{&a, 0, 0, 0, 0, false});
+    block1<OPT, SR, false>(a.s, d, lb, 0, tb, red, Prefetch1{&a, 0, 0, 0, 0, false}, static_cast<int>(threadIdx.x), 0, 0, 0u);
 }
 
 // fp32-state path: one CTA per tensor (numel < 4096 = 512 threads x 8).
@@ -327,10 +373,11 @@ template <int OPT, bool SR>
 cudaError_t launch1(const Step1Args& a, bool has_partial, cudaStream_t st)
 {
     int full = 0, unused = 0;
-    cudaError_t e = persistent_grid(reinterpret_cast<const void*>(step1_kernel<OPT, SR>), kT1, kSmem1, &full);
+    cudaError_t e = persistent_grid(reinterpret_cast<const void*>(step1_kernel<OPT, SR>), kT1 * kGroups1, kSmem1Main, &full);
     if (e != cudaSuccess) return e;
-    const int grid = a.nblocks < full ? a.nblocks : full;
-    if (grid > 0) step1_kernel<OPT, SR><<<grid, kT1, kSmem1, st>>>(a);
+    const int per = (a.nblocks + kGroups1 - 1) / kGroups1;
+    const int grid = per < full ? per : full;
+    if (grid > 0) step1_kernel<OPT, SR><<<grid, kT1 * kGroups1, kSmem1Main, st>>>(a);
     if (has_partial && a.nt > 0) {
         e = persistent_grid(reinterpret_cast<const void*>(step1_tail_kernel<OPT, SR>), kT1, kSmem1, &unused);
         if (e != cudaSuccess) return e;
