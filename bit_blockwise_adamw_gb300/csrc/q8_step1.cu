@@ -154,7 +154,7 @@ __device__ __forceinline__ float onestate(const Scalars1& s, float g, float p, f
 // id, `lead` = the thread that issues the L2 prefetch and stores the absmax,
 // `lut` = shared address of the lane-replicated codebook); FULL = sixteen
 // valid elements per thread.
-// The L2 prefetch thread 0 issues during a block: the inputs of global block
+// The L2 prefetch the leader thread issues during a block: the inputs of global block
 // `target` (when `on`), which lies in the current tensor if target < next.
 struct Prefetch1 {
     const Step1Args* a;

@@ -188,7 +188,7 @@ __device__ __forceinline__ void bar_group(int id)
     asm volatile("bar.sync %0, %1;" ::"r"(id), "n"(kT8) : "memory");
 }
 
-// The L2 prefetch thread 0 issues during a block: the inputs of global block
+// The L2 prefetch the leader thread issues during a block: the inputs of global block
 // `target` (when `on`), which lies in the current tensor if target < next.
 struct Prefetch {
     const Step8Args* a;
