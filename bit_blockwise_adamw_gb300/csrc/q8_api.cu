@@ -208,7 +208,11 @@ const char* q8_last_error(void) { return g_error.c_str(); }
 int q8_prepare_device(void)
 {
     const q8::DevTables* tab = nullptr;
-    const cudaError_t err = q8::device_tables(&tab);
+    cudaError_t err = q8::device_tables(&tab);
+    if (err == cudaSuccess) err = q8::prepare_step8();
+    if (err == cudaSuccess) err = q8::prepare_step1();
+    if (err == cudaSuccess) err = q8::prepare_step16();
+    if (err == cudaSuccess) err = q8::prepare_codec();
     if (err != cudaSuccess) return cuda_fail(err, "q8_prepare_device");
     return Q8_OK;
 }

@@ -119,6 +119,19 @@ __global__ void __launch_bounds__(kThreads) philox_fill_kernel(const __grid_cons
 
 }  // namespace
 
+cudaError_t prepare_codec()
+{
+    int g = 0;
+    const void* ks[] = {reinterpret_cast<const void*>(quantize_kernel<Q8_SIGNED>),
+                        reinterpret_cast<const void*>(quantize_kernel<Q8_UNSIGNED>),
+                        reinterpret_cast<const void*>(dequantize_kernel), reinterpret_cast<const void*>(philox_fill_kernel)};
+    for (const void* k : ks) {
+        const cudaError_t e = persistent_grid(k, kThreads, 0, &g);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_quantize(const float* x, uint8_t* codes, float* absmax, int64_t n, int kind,
                             const DevTables* tab, cudaStream_t st)
 {

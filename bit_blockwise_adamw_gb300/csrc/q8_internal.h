@@ -168,6 +168,13 @@ cudaError_t device_tables(const DevTables** out);
 // drive several devices, each get their own device's figure.
 cudaError_t persistent_grid(const void* kernel, int threads, size_t smem, int* grid);
 
+// Work out (and cache) the launch configuration of every kernel of one
+// translation unit on the current device, so that later launches do no set-up.
+cudaError_t prepare_step8();
+cudaError_t prepare_step1();
+cudaError_t prepare_step16();
+cudaError_t prepare_codec();
+
 // Launchers (one per kernel; each returns cudaGetLastError()).
 cudaError_t launch_step8(const Step8Args& a, cudaStream_t st);
 cudaError_t launch_step32(const Step32Args& a, cudaStream_t st);

@@ -398,6 +398,28 @@ cudaError_t launch1_32(const Step1_32Args& a, cudaStream_t st)
 
 }  // namespace
 
+cudaError_t prepare_step1()
+{
+    int g = 0;
+    const void* ks[] = {reinterpret_cast<const void*>(step1_kernel<kMomentum, true>),
+                        reinterpret_cast<const void*>(step1_kernel<kMomentum, false>),
+                        reinterpret_cast<const void*>(step1_kernel<kLion, true>),
+                        reinterpret_cast<const void*>(step1_kernel<kLion, false>)};
+    const void* ts[] = {reinterpret_cast<const void*>(step1_tail_kernel<kMomentum, true>),
+                        reinterpret_cast<const void*>(step1_tail_kernel<kMomentum, false>),
+                        reinterpret_cast<const void*>(step1_tail_kernel<kLion, true>),
+                        reinterpret_cast<const void*>(step1_tail_kernel<kLion, false>)};
+    for (const void* k : ks) {
+        const cudaError_t e = persistent_grid(k, kT1 * kGroups1, kSmem1Main, &g);
+        if (e != cudaSuccess) return e;
+    }
+    for (const void* k : ts) {
+        const cudaError_t e = persistent_grid(k, kT1, kSmem1, &g);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_step1(int opt, const Step1Args& a, cudaStream_t st)
 {
     bool has_partial = false;

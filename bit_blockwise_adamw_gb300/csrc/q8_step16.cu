@@ -144,6 +144,14 @@ __global__ void __launch_bounds__(kThreads, 4) step16_kernel(const __grid_consta
 
 }  // namespace
 
+cudaError_t prepare_step16()
+{
+    int g = 0;
+    cudaError_t e = persistent_grid(reinterpret_cast<const void*>(step16_kernel<true>), kThreads, 0, &g);
+    if (e == cudaSuccess) e = persistent_grid(reinterpret_cast<const void*>(step16_kernel<false>), kThreads, 0, &g);
+    return e;
+}
+
 cudaError_t launch_step16(const Step16Args& a, cudaStream_t st)
 {
     const void* k = a.s.sr ? reinterpret_cast<const void*>(step16_kernel<true>)

@@ -465,6 +465,23 @@ cudaError_t launch_step8_t(const Step8Args& a, bool has_partial, cudaStream_t st
 
 }  // namespace
 
+cudaError_t prepare_step8()
+{
+    int g = 0;
+    const void* ks[] = {reinterpret_cast<const void*>(step8_kernel<true>), reinterpret_cast<const void*>(step8_kernel<false>)};
+    const void* ts[] = {reinterpret_cast<const void*>(step8_tail_kernel<true>),
+                        reinterpret_cast<const void*>(step8_tail_kernel<false>)};
+    for (const void* k : ks) {
+        const cudaError_t e = persistent_grid(k, kT8 * kGroups, kSmemBytes, &g);
+        if (e != cudaSuccess) return e;
+    }
+    for (const void* k : ts) {
+        const cudaError_t e = persistent_grid(k, kT8, kTailSmemBytes, &g);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+
 cudaError_t launch_step8(const Step8Args& a, cudaStream_t st)
 {
     bool has_partial = false;

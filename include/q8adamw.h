@@ -247,9 +247,11 @@ int q8_selftest_sqrt_div(uint64_t* counts, q8_stream_t stream);
 
 /*
  * One-time set-up of the current device: uploads the codebooks and search
- * tables and waits for the copy (a device-wide synchronisation).  Every
- * other entry point calls it on first use; call it yourself before capturing
- * a CUDA graph or when the first step must not synchronise.
+ * tables and waits for the copy (a device-wide synchronisation), then works
+ * out and caches the launch configuration of every kernel of the library on
+ * this device.  Every other entry point does the part it needs on first use;
+ * call this yourself before capturing a CUDA graph or when the first step
+ * must not synchronise.
  */
 int q8_prepare_device(void);
 
