@@ -123,6 +123,34 @@ def _replay16(job):
     return st.param, st.m, st.v
 
 
+def _replay1(job):
+    """Oracle replay of one block of a one-state step (8-bit m), or of a whole
+    small tensor (fp32 m): job = (param0, grads[steps], E0, (opt, hps, eight_bit))."""
+    p0, grads, e0, (opt, hps, eight_bit) = job
+    st = o.zeros_onestate(p0.copy(), grads[0], eight_bit=eight_bit)
+    if eight_bit:
+        st.m_absmax = np.zeros(1, np.float32)
+    for g, h in zip(grads, hps):
+        st.grad = g
+        if eight_bit:
+            o.onestate8bit_tensor(opt, st, e0, o.hparams(**h))
+        else:
+            o.onestate32_tensor(opt, st, e0, o.hparams(**h))
+    return (st.param, st.m_codes, st.m_absmax) if eight_bit else (st.param, st.m32)
+
+
+def onestate_hp(opt, wl, step, sr=1):
+    """Hyper-parameters of the one-state steps on a workload, as the bench
+    times them: Momentum with momentum beta1; Lion with lr/10, beta1 and 0.99;
+    the workload's weight decay.  Returned as oracle keyword arguments."""
+    h = wl.hp
+    if opt == o.MOMENTUM:
+        return dict(lr=h["lr"], beta1=h["beta1"], weight_decay=h["weight_decay"], step=step,
+                    seed=wl.philox_seed, sr=sr)
+    return dict(lr=h["lr"] / 10, beta1=h["beta1"], beta2=0.99, weight_decay=h["weight_decay"], step=step,
+                seed=wl.philox_seed, sr=sr)
+
+
 def oracle_pool(processes=None):
     return mp.get_context("spawn").Pool(processes)
 
@@ -131,8 +159,9 @@ class SampledRun:
     """Run a full-size workload on the GPU while recording the inputs of the
     sampled blocks (and of every small tensor) for an oracle replay."""
 
-    def __init__(self, wl, device, fraction, steps=None, extra_blocks=()):
+    def __init__(self, wl, device, fraction, steps=None, extra_blocks=(), opt=None):
         self.wl = wl
+        self.opt = opt                  # None: AdamW; o.MOMENTUM or o.LION: the one-state step
         self.steps = steps or wl.steps
         self.device = device
         self.picks = sorted(set(W.sample_blocks(wl, fraction)) | set(extra_blocks))
@@ -172,7 +201,9 @@ class SampledRun:
         self.p0 = self._slices(params)
         self.grads = []
         self.hps = []
-        if wl.state == "8bit":
+        if self.opt is not None:
+            states = [q8.Tensor8.zeros_like(p, None, moments=1) for p in params]
+        elif wl.state == "8bit":
             states = gpu_states8(params)
         else:
             states = [q8.Tensor16(p, None, torch.zeros_like(p), torch.zeros_like(p)) for p in params]
@@ -182,8 +213,15 @@ class SampledRun:
             for s, g in zip(states, grads):
                 s.grad = g
             packed = q8.pack_tensor8(states) if wl.state == "8bit" else q8.pack_tensor16(states)
-            h = hp_for(wl, step)
-            if wl.state == "8bit":
+            h = hp_for(wl, step) if self.opt is None else onestate_hp(self.opt, wl, step)
+            if self.opt == o.MOMENTUM:
+                q8.momentum8bit_sr_step(packed, q8.momentum_hparams(
+                    lr=h["lr"], momentum=h["beta1"], weight_decay=h["weight_decay"], step=step, seed=h["seed"]))
+            elif self.opt == o.LION:
+                q8.lion8bit_sr_step(packed, q8.lion_hparams(
+                    lr=h["lr"], beta1=h["beta1"], beta2=h["beta2"], weight_decay=h["weight_decay"], step=step,
+                    seed=h["seed"]))
+            elif wl.state == "8bit":
                 q8.adamw8bit_sr_step(packed, q8.hparams(**h))
             else:
                 q8.adamw_bf16_sr_step(packed, q8.hparams(**h))
@@ -194,7 +232,13 @@ class SampledRun:
         self.final = {}
         npy = lambda t: t.cpu().numpy()
         fp = self._gather([s.param for s in states], u16)
-        if wl.state == "8bit":
+        if self.opt is not None:
+            fm = self._gather([s.m_codes if s.m_codes is not None else s.param for s in states], npy)
+            for i, b in self.picks:
+                self.final[(i, b)] = (fp[(i, b)], fm[(i, b)], npy(states[i].m_absmax[b:b + 1]))
+            for i in self.small:
+                self.final[(i, -1)] = (u16(states[i].param), states[i].m32.cpu().numpy())
+        elif wl.state == "8bit":
             fm = self._gather([s.m_codes if s.m_codes is not None else s.param for s in states], npy)
             fv = self._gather([s.v_codes if s.v_codes is not None else s.param for s in states], npy)
             for i, b in self.picks:
@@ -206,7 +250,7 @@ class SampledRun:
             fv = self._gather([s.v for s in states], u16)
             for k in self.picks:
                 self.final[k] = (fp[k], fm[k], fv[k])
-        for i in self.small:
+        for i in self.small if self.opt is None else []:
             s = states[i]
             self.final[(i, -1)] = (u16(s.param), s.m32.cpu().numpy(), s.v32.cpu().numpy())
         del states, params
@@ -218,7 +262,8 @@ class SampledRun:
         for k in keys:
             i, b = k
             e0 = self.offsets[i] + (b * BLOCK if b >= 0 else 0)
-            out.append((k, (self.p0[k], [g[k] for g in self.grads], e0, self.hps)))
+            extra = self.hps if self.opt is None else (self.opt, self.hps, b >= 0)
+            out.append((k, (self.p0[k], [g[k] for g in self.grads], e0, extra)))
         return out
 
     def check(self, pool):
@@ -227,7 +272,9 @@ class SampledRun:
         jobs = self.jobs()
         fns = []
         for k, job in jobs:
-            if k[1] == -1:
+            if self.opt is not None:
+                fns.append(_replay1)
+            elif k[1] == -1:
                 fns.append(_replay32)
             elif self.wl.state == "8bit":
                 fns.append(_replay8)
@@ -238,7 +285,7 @@ class SampledRun:
         for (k, _), r in zip(jobs, results):
             want = r.get()
             got = self.final[k]
-            names = ("param", "m", "v", "m_absmax", "v_absmax")
+            names = ("param", "m", "v", "m_absmax", "v_absmax") if self.opt is None else ("param", "m", "m_absmax")
             for name, gv, wv in zip(names, got, want):
                 gv = np.asarray(gv)
                 wv = np.asarray(wv)

@@ -8,7 +8,7 @@ import bit_blockwise_adamw_gb300 as q8
 from bit_blockwise_adamw_gb300 import workloads as W
 import oracle as o
 
-from parity import compare_slice8, host_slice8, u16
+from parity import SampledRun, compare_slice8, host_slice8, oracle_pool, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -138,3 +138,22 @@ def test_sharded_step_equals_unsharded(cuda_device, name):
             assert torch.equal(a.m_codes, b.m_codes) and torch.equal(a.m_absmax, b.m_absmax)
         else:
             assert torch.equal(a.m32, b.m32)
+
+
+@pytest.fixture(scope="module")
+def pool():
+    p = oracle_pool()
+    yield p
+    p.close()
+    p.join()
+
+
+@pytest.mark.parametrize("name", ["momentum", "lion"])
+def test_full_size_sampled_parity_gptneo67b(cuda_device, pool, name):
+    """The GPT-Neo 6.7B list at full size, launched as the benchmark launches
+    it (one call per step, the bench's hyper-parameters): a seeded sample of
+    blocks plus the first and last block of every tensor, replayed by the
+    oracle over three steps, bit for bit."""
+    run = SampledRun(W.WORKLOADS["gptneo-6.7b"], cuda_device, 0.002, steps=3, opt=OPTS[name][0])
+    run.run()
+    assert run.check(pool) > 0
