@@ -67,6 +67,13 @@ class _FrontEnd(torch.optim.Optimizer):
         super().__init__(params, defaults)
         self._next_offset = 0
         self._tables = {}
+        # the library's one-time per-device set-up (tables, launch
+        # configurations) now, so that no step synchronises or does set-up
+        # (a step may then be captured in a CUDA graph)
+        devices = {p.device for g in self.param_groups for p in g["params"] if p.is_cuda}
+        for dev in devices:
+            with torch.cuda.device(dev):
+                B.q8_prepare_device()
 
     def _offset(self, p, state):
         if "philox_offset" not in state:
