@@ -162,7 +162,22 @@ struct Prefetch1 {
     bool on;
 };
 
-template <int OPT, bool SR, bool FULL>
+// 32-byte streaming load and store (sixteen bf16 values), for launches whose
+// grad and param arrays are all 32-byte aligned.
+__device__ __forceinline__ void ld32_1(const void* p, uint32_t (&w)[8])
+{
+    asm volatile("ld.global.cs.v8.u32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+                 : "=r"(w[0]), "=r"(w[1]), "=r"(w[2]), "=r"(w[3]), "=r"(w[4]), "=r"(w[5]), "=r"(w[6]), "=r"(w[7])
+                 : "l"(p));
+}
+__device__ __forceinline__ void st32_1(void* p, const uint32_t (&w)[8])
+{
+    asm volatile("st.global.cs.v8.u32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};"
+                 ::"l"(p), "r"(w[0]), "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+                 : "memory");
+}
+
+template <int OPT, bool SR, bool FULL, bool W32 = false>
 __device__ __forceinline__ void block1(const Scalars1& s, const Desc8& d, int lb, int it, const Tables1* tb,
                                        uint32_t* red2, const Prefetch1& pf, int tid, int bar, int lead, uint32_t lut)
 {
@@ -174,11 +189,16 @@ __device__ __forceinline__ void block1(const Scalars1& s, const Desc8& d, int lb
 
     uint32_t gw[8], pw[8], mc[4];
     if constexpr (FULL) {
-        const uint4 g0 = ld_stream16(d.g + i0), g1 = ld_stream16(d.g + i0 + 8);
-        const uint4 p0 = ld_stream16(d.p + i0), p1 = ld_stream16(d.p + i0 + 8);
+        if constexpr (W32) {
+            ld32_1(d.g + i0, gw);
+            ld32_1(d.p + i0, pw);
+        } else {
+            const uint4 g0 = ld_stream16(d.g + i0), g1 = ld_stream16(d.g + i0 + 8);
+            const uint4 p0 = ld_stream16(d.p + i0), p1 = ld_stream16(d.p + i0 + 8);
+            gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w; gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
+            pw[0] = p0.x; pw[1] = p0.y; pw[2] = p0.z; pw[3] = p0.w; pw[4] = p1.x; pw[5] = p1.y; pw[6] = p1.z; pw[7] = p1.w;
+        }
         const uint4 mq = ld_stream16(d.mq + i0);
-        gw[0] = g0.x; gw[1] = g0.y; gw[2] = g0.z; gw[3] = g0.w; gw[4] = g1.x; gw[5] = g1.y; gw[6] = g1.z; gw[7] = g1.w;
-        pw[0] = p0.x; pw[1] = p0.y; pw[2] = p0.z; pw[3] = p0.w; pw[4] = p1.x; pw[5] = p1.y; pw[6] = p1.z; pw[7] = p1.w;
         mc[0] = mq.x; mc[1] = mq.y; mc[2] = mq.z; mc[3] = mq.w;
         // after this block's own loads are in flight
         if (tid == lead && pf.on) {
@@ -227,8 +247,12 @@ __device__ __forceinline__ void block1(const Scalars1& s, const Desc8& d, int lb
         po[k] = round2<SR>(onestate2<OPT>(s, bf16x2(gw[k]), bf16x2(pw[k]), m[k]), r[k]);
     }
     if constexpr (FULL) {
-        st_stream16(d.p + i0, make_uint4(po[0], po[1], po[2], po[3]));
-        st_stream16(d.p + i0 + 8, make_uint4(po[4], po[5], po[6], po[7]));
+        if constexpr (W32) {
+            st32_1(d.p + i0, po);
+        } else {
+            st_stream16(d.p + i0, make_uint4(po[0], po[1], po[2], po[3]));
+            st_stream16(d.p + i0 + 8, make_uint4(po[4], po[5], po[6], po[7]));
+        }
     } else {
 #pragma unroll
         for (int k = 0; k < 8; ++k) {
@@ -275,7 +299,7 @@ __device__ __forceinline__ bool partial1(const Desc8& d, int lb)
     return static_cast<int64_t>(lb + 1) * kBlock > d.n;
 }
 
-template <int OPT, bool SR>
+template <int OPT, bool SR, bool W32>
 __global__ void __launch_bounds__(kT1 * kGroups1, 1) step1_kernel(const __grid_constant__ Step1Args a)
 {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -317,7 +341,7 @@ __global__ void __launch_bounds__(kT1 * kGroups1, 1) step1_kernel(const __grid_c
         const int next = a.blk_start[ti + 1];
         const int full_end = min(min(end, next), base + static_cast<int>(d.n / kBlock));
         for (; gb < full_end; ++gb)
-            block1<OPT, SR, true>(a.s, d, gb - base, it++, tb, red, Prefetch1{&a, gb + kAhead, next, base, ti, gb + kAhead < end},
+            block1<OPT, SR, true, W32>(a.s, d, gb - base, it++, tb, red, Prefetch1{&a, gb + kAhead, next, base, ti, gb + kAhead < end},
                                   tid, 1 + grp, lead, lut);
         gb = min(end, next);
     }
@@ -369,15 +393,15 @@ __global__ void __launch_bounds__(kSmall1) step1_32_kernel(const __grid_constant
     }
 }
 
-template <int OPT, bool SR>
+template <int OPT, bool SR, bool W32>
 cudaError_t launch1(const Step1Args& a, bool has_partial, cudaStream_t st)
 {
     int full = 0, unused = 0;
-    cudaError_t e = persistent_grid(reinterpret_cast<const void*>(step1_kernel<OPT, SR>), kT1 * kGroups1, kSmem1Main, &full);
+    cudaError_t e = persistent_grid(reinterpret_cast<const void*>(step1_kernel<OPT, SR, W32>), kT1 * kGroups1, kSmem1Main, &full);
     if (e != cudaSuccess) return e;
     const int per = (a.nblocks + kGroups1 - 1) / kGroups1;
     const int grid = per < full ? per : full;
-    if (grid > 0) step1_kernel<OPT, SR><<<grid, kT1 * kGroups1, kSmem1Main, st>>>(a);
+    if (grid > 0) step1_kernel<OPT, SR, W32><<<grid, kT1 * kGroups1, kSmem1Main, st>>>(a);
     if (has_partial && a.nt > 0) {
         e = persistent_grid(reinterpret_cast<const void*>(step1_tail_kernel<OPT, SR>), kT1, kSmem1, &unused);
         if (e != cudaSuccess) return e;
@@ -401,10 +425,14 @@ cudaError_t launch1_32(const Step1_32Args& a, cudaStream_t st)
 cudaError_t prepare_step1()
 {
     int g = 0;
-    const void* ks[] = {reinterpret_cast<const void*>(step1_kernel<kMomentum, true>),
-                        reinterpret_cast<const void*>(step1_kernel<kMomentum, false>),
-                        reinterpret_cast<const void*>(step1_kernel<kLion, true>),
-                        reinterpret_cast<const void*>(step1_kernel<kLion, false>)};
+    const void* ks[] = {reinterpret_cast<const void*>(step1_kernel<kMomentum, true, true>),
+                        reinterpret_cast<const void*>(step1_kernel<kMomentum, true, false>),
+                        reinterpret_cast<const void*>(step1_kernel<kMomentum, false, true>),
+                        reinterpret_cast<const void*>(step1_kernel<kMomentum, false, false>),
+                        reinterpret_cast<const void*>(step1_kernel<kLion, true, true>),
+                        reinterpret_cast<const void*>(step1_kernel<kLion, true, false>),
+                        reinterpret_cast<const void*>(step1_kernel<kLion, false, true>),
+                        reinterpret_cast<const void*>(step1_kernel<kLion, false, false>)};
     const void* ts[] = {reinterpret_cast<const void*>(step1_tail_kernel<kMomentum, true>),
                         reinterpret_cast<const void*>(step1_tail_kernel<kMomentum, false>),
                         reinterpret_cast<const void*>(step1_tail_kernel<kLion, true>),
@@ -422,11 +450,17 @@ cudaError_t prepare_step1()
 
 cudaError_t launch_step1(int opt, const Step1Args& a, cudaStream_t st)
 {
-    bool has_partial = false;
-    for (int i = 0; i < a.nt; ++i) has_partial = has_partial || (a.d[i].n % kBlock) != 0;
-    if (opt == kMomentum)
-        return a.s.sr ? launch1<kMomentum, true>(a, has_partial, st) : launch1<kMomentum, false>(a, has_partial, st);
-    return a.s.sr ? launch1<kLion, true>(a, has_partial, st) : launch1<kLion, false>(a, has_partial, st);
+    bool has_partial = false, w32 = true;
+    for (int i = 0; i < a.nt; ++i) {
+        has_partial = has_partial || (a.d[i].n % kBlock) != 0;
+        w32 = w32 && (reinterpret_cast<uintptr_t>(a.d[i].g) % 32) == 0 && (reinterpret_cast<uintptr_t>(a.d[i].p) % 32) == 0;
+    }
+    if (opt == kMomentum) {
+        if (a.s.sr) return w32 ? launch1<kMomentum, true, true>(a, has_partial, st) : launch1<kMomentum, true, false>(a, has_partial, st);
+        return w32 ? launch1<kMomentum, false, true>(a, has_partial, st) : launch1<kMomentum, false, false>(a, has_partial, st);
+    }
+    if (a.s.sr) return w32 ? launch1<kLion, true, true>(a, has_partial, st) : launch1<kLion, true, false>(a, has_partial, st);
+    return w32 ? launch1<kLion, false, true>(a, has_partial, st) : launch1<kLion, false, false>(a, has_partial, st);
 }
 
 cudaError_t launch_step1_32(int opt, const Step1_32Args& a, cudaStream_t st)
