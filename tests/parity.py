@@ -24,6 +24,16 @@ def hp_for(wl, step, sr=1):
                 weight_decay=h["weight_decay"], step=step, seed=wl.philox_seed, sr=sr)
 
 
+def shift16(t):
+    """A copy of the 1-D tensor t whose data starts 16 bytes past a 32-byte
+    boundary (allowed by the ABI's 16-byte rule, but not 32-byte aligned)."""
+    buf = torch.empty(t.numel() + 16 // t.element_size(), dtype=t.dtype, device=t.device)
+    v = buf[16 // t.element_size():]
+    v.copy_(t)
+    assert v.data_ptr() % 32 == 16
+    return v
+
+
 def gpu_states8(params, offsets=None):
     offsets = offsets or [-1] * len(params)
     return [q8.Tensor8.zeros_like(p, None, philox_offset=off) for p, off in zip(params, offsets)]

@@ -8,7 +8,7 @@ import bit_blockwise_adamw_gb300 as q8
 from bit_blockwise_adamw_gb300 import workloads as W
 import oracle as o
 
-from parity import SampledRun, compare_slice8, host_slice8, oracle_pool, u16
+from parity import SampledRun, compare_slice8, host_slice8, oracle_pool, shift16, u16
 
 pytestmark = pytest.mark.gpu
 
@@ -23,15 +23,17 @@ def _hp(name, step, sr, wd=0.01):
             o.hparams(lr=1e-4, beta1=0.9, beta2=0.99, weight_decay=wd, step=step, seed=3, sr=sr))
 
 
-def _run(name, wl, device, steps, sr=1, offsets=None, grad_hook=None, wd=0.01):
+def _run(name, wl, device, steps, sr=1, offsets=None, grad_hook=None, wd=0.01, shifted=()):
     opt, fn = OPTS[name]
     params = W.init_params(wl, device)
+    params = [shift16(p) if i in shifted else p for i, p in enumerate(params)]
     offsets = offsets or [-1] * len(params)
     gpu = [q8.Tensor8.zeros_like(p, None, philox_offset=off, moments=1) for p, off in zip(params, offsets)]
     host = [o.zeros_onestate(u16(p), np.zeros(p.numel(), np.uint16), philox_offset=off)
             for p, off in zip(params, offsets)]
     for step in range(1, steps + 1):
         grads = W.make_grads(wl, step, device)
+        grads = [shift16(g) if i in shifted else g for i, g in enumerate(grads)]
         if grad_hook:
             grad_hook(step, grads)
         for a, b, g in zip(gpu, host, grads):
@@ -84,6 +86,15 @@ def test_zero_gradient_blocks(cuda_device, name):
 def test_misaligned_offsets(cuda_device, name):
     wl = W.custom("offs", [5000, 2048 * 3 + 5, 700], steps=3, data_seed=92)
     _run(name, wl, cuda_device, 3, offsets=[3, (1 << 33) + 5, 11])
+
+
+@pytest.mark.parametrize("name", ["momentum", "lion"])
+@pytest.mark.parametrize("shifted", [(0, 1, 2), (1,)], ids=["all", "one"])
+def test_grad_and_param_16_byte_aligned(cuda_device, name, shifted):
+    """Grad and param arrays 16-byte but not 32-byte aligned: 16-byte accesses
+    instead of 32-byte ones, the same results."""
+    wl = W.custom("shift16", [2048 * 30, 2048 * 5 + 9, 3000], steps=3, data_seed=94)
+    _run(name, wl, cuda_device, 3, shifted=shifted)
 
 
 @pytest.mark.parametrize("name", ["momentum", "lion"])

@@ -16,7 +16,7 @@ from bit_blockwise_adamw_gb300 import workloads as W
 import oracle as o
 
 from parity import (SampledRun, compare_slice8, compare_state8, gpu_states8, host_slice8, host_states8, hp_for,
-                    oracle_pool, u16)
+                    oracle_pool, shift16, u16)
 
 pytestmark = pytest.mark.gpu
 
@@ -29,18 +29,21 @@ def pool():
     p.join()
 
 
-def _run_full(wl, device, steps=None, sr=1, offsets=None, split=None, grad_hook=None, param_hook=None):
+def _run_full(wl, device, steps=None, sr=1, offsets=None, split=None, grad_hook=None, param_hook=None, shifted=()):
     """Run `wl` on both sides for `steps`, comparing everything after each step
     (`grad_hook(step, grads)` may edit the step's gradients in place first,
-    `param_hook(params)` the initial parameters)."""
+    `param_hook(params)` the initial parameters; the params and grads of the
+    tensors in `shifted` sit 16 bytes past a 32-byte boundary)."""
     steps = steps or wl.steps
     params = W.init_params(wl, device)
+    params = [shift16(p) if i in shifted else p for i, p in enumerate(params)]
     if param_hook:
         param_hook(params)
     gpu = gpu_states8(params, offsets)
     host = host_states8([u16(p) for p in params], offsets)
     for step in range(1, steps + 1):
         grads = W.make_grads(wl, step, device)
+        grads = [shift16(g) if i in shifted else g for i, g in enumerate(grads)]
         if grad_hook:
             grad_hook(step, grads)
         for g_gpu, g_host, gr in zip(gpu, host, grads):
@@ -124,6 +127,17 @@ def test_explicit_misaligned_offsets(cuda_device):
     sizes = [5000, 4099, 700, 2048 * 5 + 3]
     wl = W.custom("offsets", sizes, steps=3, data_seed=78)
     _run_full(wl, cuda_device, offsets=[3, 1 << 33, 12345677, 7])
+
+
+@pytest.mark.parametrize("sr", [1, 0])
+@pytest.mark.parametrize("shifted", [(0, 1, 2, 3), (2,)], ids=["all", "one"])
+def test_grad_and_param_16_byte_aligned(cuda_device, sr, shifted):
+    """Grad and param arrays 16-byte but not 32-byte aligned (all of them, or
+    one tensor of the list): the launch then moves grad and param with 16-byte
+    accesses instead of 32-byte ones; the results are the oracle's all the same."""
+    sizes = [2048 * 40, 2048 * 7 + 5, 5000, 1000]
+    wl = W.custom("shift16", sizes, steps=3, data_seed=83, grad_std=1e-3)
+    _run_full(wl, cuda_device, sr=sr, shifted=shifted)
 
 
 def test_split_list_equals_whole_list(cuda_device):
