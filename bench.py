@@ -55,8 +55,10 @@ def parse():
     ap.add_argument("--secondary-steps", type=int, default=10)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=3)
-    ap.add_argument("--cpu-blocks", type=int, default=24000,
-                    help="2048-blocks in the oracle's timed sample (about 10-20 s on one core)")
+    ap.add_argument("--cpu-blocks", type=int, default=100000,
+                    help="2048-blocks in the oracle's single-core timed sample (about 20 s on one core)")
+    ap.add_argument("--cpu-blocks-per-proc", type=int, default=6000,
+                    help="2048-blocks per process in the oracle's block-parallel timing")
     return ap.parse_args()
 
 
@@ -179,38 +181,82 @@ def traffic_per_launch(kernel, units):
 
 # ---------------------------------------------------------------- CPU oracle
 
-def _oracle_sample(wl, nblocks, seed):
-    """A seeded sample of the workload's 2048-blocks as oracle states, and a
-    function that runs one step of the oracle over them; returns (params, run)."""
+def sample_runs(wl, nblocks, rng, run_blocks=512):
+    """The oracle sample's layout: (tensor index, first block, blocks) runs of
+    consecutive full 2048-blocks, tensors drawn in proportion to their size
+    among those on the 8-bit path (all of them for BF16 state), `nblocks`
+    blocks in all."""
+    bigs = [i for i, t in enumerate(wl.tensors) if t.numel >= 4096 or wl.state == "bf16"]
+    sizes = np.array([wl.tensors[i].numel for i in bigs], np.float64)
+    runs, left = [], nblocks
+    while left > 0:
+        i = bigs[rng.choice(len(bigs), p=sizes / sizes.sum())]
+        full = max(1, wl.tensors[i].numel // BLOCK)
+        n = min(run_blocks, left, full)
+        runs.append((i, int(rng.integers(0, full - n + 1)), n))
+        left -= n
+    return runs
+
+
+def _oracle_sample(wl, nblocks, seed, run_blocks=512):
+    """A seeded sample of the workload's 2048-blocks as oracle states, in runs
+    of up to `run_blocks` consecutive full blocks of one tensor (so that the
+    oracle's per-call set-up, its codebooks and midpoints, weighs as little as
+    in a whole-tensor call), and a function that runs one step of the oracle
+    over them with each run's global Philox offset; returns (params, run)."""
     import oracle as o
     from bit_blockwise_adamw_gb300 import workloads as W
     rng = np.random.default_rng(seed)
-    bigs = [i for i, t in enumerate(wl.tensors) if t.numel >= 4096 or wl.state == "bf16"]
-    sizes = np.array([wl.tensors[i].numel for i in bigs], np.float64)
-    pick = rng.choice(len(bigs), size=nblocks, p=sizes / sizes.sum())
+    offs = W.philox_offsets(wl)
     # inputs of the sample: N(0, 0.02) params and the workload's grad law
     gen = torch.Generator().manual_seed(seed)
-    p = (torch.randn(nblocks * BLOCK, generator=gen) * 0.02).to(torch.bfloat16)
-    g = (torch.randn(nblocks * BLOCK, generator=gen) * wl.grad_std).to(torch.bfloat16)
-    p = p.view(torch.int16).numpy().view(np.uint16).reshape(nblocks, BLOCK)
-    g = g.view(torch.int16).numpy().view(np.uint16).reshape(nblocks, BLOCK)
-    offs = W.philox_offsets(wl)
+
+    def bits(x):
+        return x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+
     h = dict(wl.hp)
     hp = o.hparams(lr=h["lr"], beta1=h["beta1"], beta2=h["beta2"], eps=h["eps"],
                    weight_decay=h["weight_decay"], step=1, seed=wl.philox_seed)
-    if wl.state == "bf16":
-        states = [o.State16(p[k].copy(), g[k].copy(), np.zeros(BLOCK, np.uint16), np.zeros(BLOCK, np.uint16))
-                  for k in range(nblocks)]
-        one = o.adamw_bf16_tensor
-    else:
-        states = [o.State8.zeros(p[k].copy(), g[k].copy(), eight_bit=True) for k in range(nblocks)]
-        one = o.adamw8bit_tensor
-    e0 = [offs[bigs[pick[k]]] for k in range(nblocks)]
+    states, e0 = [], []
+    for i, b0, n in sample_runs(wl, nblocks, rng, run_blocks):
+        p = bits(torch.randn(n * BLOCK, generator=gen) * 0.02)
+        g = bits(torch.randn(n * BLOCK, generator=gen) * wl.grad_std)
+        if wl.state == "bf16":
+            z = np.zeros(n * BLOCK, np.uint16)
+            states.append(o.State16(p, g, z, z.copy()))
+        else:
+            states.append(o.State8.zeros(p, g, eight_bit=True))
+        e0.append(offs[i] + b0 * BLOCK)
+    one = o.adamw_bf16_tensor if wl.state == "bf16" else o.adamw8bit_tensor
 
     def run():
-        for k, st in enumerate(states):
-            one(st, e0[k], hp)
+        for st, e in zip(states, e0):
+            one(st, e, hp)
     return nblocks * BLOCK, run
+
+
+def oracle_flat1m_time(device):
+    """Time the oracle (single-threaded C) over the whole flat 1,048,576-param
+    workload, all its steps (fresh gradients each step, made on the GPU and
+    copied to the host before the clock starts); returns (param-steps, seconds)."""
+    import oracle as o
+    from bit_blockwise_adamw_gb300 import workloads as W
+    wl = W.WORKLOADS["flat-1m"]
+    params = [p.view(torch.int16).cpu().numpy().view(np.uint16) for p in W.init_params(wl, device)]
+    grads = [[g.view(torch.int16).cpu().numpy().view(np.uint16) for g in W.make_grads(wl, t, device)]
+             for t in range(1, wl.steps + 1)]
+    states = [o.State8.zeros(p.copy(), np.zeros_like(p)) for p in params]
+    h = dict(wl.hp)
+    dt = 0.0
+    for t in range(1, wl.steps + 1):
+        for st, g in zip(states, grads[t - 1]):
+            st.grad = g
+        hp = o.hparams(lr=h["lr"], beta1=h["beta1"], beta2=h["beta2"], eps=h["eps"],
+                       weight_decay=h["weight_decay"], step=t, seed=wl.philox_seed)
+        t0 = time.perf_counter()
+        o.adamw8bit_sr_step(states, hp)
+        dt += time.perf_counter() - t0
+    return sum(p.size for p in params) * wl.steps, dt
 
 
 def oracle_sample_time(wl, nblocks, seed=0):
@@ -271,7 +317,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic", "config": {"workload": wl.name, "sample_blocks_per_step": nblocks},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": "%d seeded 2048-blocks of %s per step, one step each" % (nblocks, wl.name)},
+                         "sample": "%d seeded 2048-blocks of %s per step in runs of up to 512 consecutive blocks, one step each" % (nblocks, wl.name)},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -402,15 +448,19 @@ def main():
     if not args.no_cpu_baseline and rank == 0 and args.optimizer == "adamw":
         n, dt = oracle_sample_time(wl, args.cpu_blocks)
         cpu = {"value": n / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
-               "sample": "%d seeded 2048-blocks (%d params) of %s, one step, single-threaded C oracle"
+               "sample": "%d seeded 2048-blocks (%d params) of %s in runs of up to 512 consecutive blocks, one step, single-threaded C oracle"
                          % (args.cpu_blocks, n, wl.name)}
+        n, dt = oracle_flat1m_time(device)
+        cpu["flat_1m"] = {"value": n / dt / 1e9, "unit": UNIT, "cores": 1, "kind": "oracle",
+                          "sample": "the whole flat-1m workload (1,048,576 params), all %d steps, single-threaded C oracle"
+                                    % (n // 1048576)}
         procs = len(os.sched_getaffinity(0))
         if procs > 1:
-            per = max(1, args.cpu_blocks // 4)
+            per = max(1, args.cpu_blocks_per_proc)
             n, dt = oracle_parallel_time(wl, per, procs)
             cpu["block_parallel"] = {
                 "value": n / dt / 1e9, "unit": UNIT, "cores": procs, "kind": "oracle",
-                "sample": "%d processes x %d seeded 2048-blocks (%d params) of %s, one step each, started together"
+                "sample": "%d processes x %d seeded 2048-blocks (%d params) of %s in runs of up to 512 consecutive blocks, one step each, started together"
                           % (procs, per, n, wl.name)}
 
     if rank == 0:

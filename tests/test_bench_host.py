@@ -1,11 +1,12 @@
 """Host-side logic of bench.py (no GPU): the algorithmic byte model, the
-launch count per step, the block-parallel oracle timing and the reference
+launch count per step, the oracle sample's layout and timing and the reference
 arm's JSON line."""
 import json
 import os
 import subprocess
 import sys
 
+import numpy as np
 import pytest
 
 import bench
@@ -47,6 +48,20 @@ def test_block_parallel_oracle_timing():
     wl = W.WORKLOADS["gptneo-6.7b"]
     n, dt = bench.oracle_parallel_time(wl, 16, 2)
     assert n == 2 * 16 * 2048 and dt > 0
+
+
+@pytest.mark.parametrize("name", ["gptneo-6.7b", "gpt2-350m", "gptneo-2.7b-bf16"])
+def test_oracle_sample_runs(name):
+    """The oracle's timed sample: runs of consecutive full blocks inside one
+    tensor each, only tensors on the 8-bit path, the requested block count."""
+    wl = W.WORKLOADS[name]
+    runs = bench.sample_runs(wl, 5000, np.random.default_rng(3), 512)
+    assert sum(n for _, _, n in runs) == 5000
+    for i, b0, n in runs:
+        t = wl.tensors[i]
+        assert 1 <= n <= 512 and b0 >= 0 and (b0 + n) * 2048 <= max(t.numel, 2048)
+        assert t.numel >= 4096 or wl.state == "bf16"
+    assert len({i for i, _, _ in runs}) > 5
 
 
 def test_reference_arm_line():
