@@ -13,7 +13,8 @@
 // partial last block of a tensor (if its length is not a multiple of 2048)
 // goes to a small second kernel, so the hot loop has only full-block code.
 // Per block each of a group's 128 threads owns sixteen contiguous elements:
-// 16-byte streaming loads of grad, param and both code arrays.  The kernel is
+// streaming loads of grad and param (32 bytes each when the launch's arrays
+// allow it, else two 16-byte loads) and of both code arrays.  The kernel is
 // bound by instruction issue rather than by DRAM, so the loop is written to
 // keep the instruction count down: packed fp32x2 arithmetic (with a packed
 // exact square root and division wherever a thread's values allow it),
