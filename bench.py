@@ -49,6 +49,9 @@ def parse():
                     help="bf16 writes: stochastic rounding (the method) or round-to-nearest-even")
     ap.add_argument("--optimizer", default="adamw", choices=["adamw", "momentum", "lion"],
                     help="8-bit-state optimizer of the step (adamw is the headline)")
+    ap.add_argument("--exact", action="store_true",
+                    help="AdamW in the bit-exact mode (correctly rounded square root and division) instead of "
+                         "the fast mode; the other mode is timed in the secondary entries either way")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
                     help="skip the BF16-state, Momentum and Lion timings that follow the headline")
@@ -381,7 +384,8 @@ def main():
             return q8.lion_hparams(lr=h["lr"], beta1=h["beta1"], beta2=0.99, weight_decay=h["weight_decay"],
                                    step=t, seed=wl.philox_seed, sr=sr)
         return q8.hparams(lr=h["lr"], beta1=h["beta1"], beta2=h["beta2"], eps=h["eps"],
-                          weight_decay=h["weight_decay"], step=t, seed=wl.philox_seed, sr=sr)
+                          weight_decay=h["weight_decay"], step=t, seed=wl.philox_seed, sr=sr,
+                          exact=int(args.exact))
 
     stream = torch.cuda.current_stream(device)
     t = 0
@@ -470,6 +474,7 @@ def main():
             "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "storage_dtype": "bf16+u8" if wl.state == "8bit" else "bf16", "data": "synthetic",
             "config": {"workload": wl.name, "optimizer": args.optimizer, "rounding": args.rounding,
+                       "mode": ("exact" if args.exact else "fast") if args.optimizer == "adamw" else "exact",
                        "params": numel, "tensors": len(wl.tensors),
                        "blocks": wl.blocks(), "state": wl.state,
                        "bytes_per_step": abytes, "gbs": abytes / (ms_per_step / 1e3) / 1e9,
@@ -505,11 +510,12 @@ def _time_steps(fn, steps, warmup, stream, device, barrier):
 
 
 def run_secondary(args, wl8, states8, peak, device, world, barrier):
-    """BF16-state AdamW on the GPT-Neo 2.7B list, 8-bit Momentum and 8-bit
-    Lion on the 6.7B list (using the headline's parameters, gradients and m
-    state), each with the headline's warm-up and events, one launch per step.
-    Per entry: ms/step, Gparams/s, algorithmic GB/s and the fraction of the
-    measured HBM peak."""
+    """The headline's 8-bit AdamW step in its other mode (bit-exact or fast),
+    BF16-state AdamW on the GPT-Neo 2.7B list (in the headline's mode), 8-bit
+    Momentum and 8-bit Lion on the 6.7B list (using the headline's parameters,
+    gradients and state), each with the headline's warm-up and events, one
+    launch per step.  Per entry: ms/step, Gparams/s, algorithmic GB/s and the
+    fraction of the measured HBM peak."""
     import bit_blockwise_adamw_gb300 as q8
     from bit_blockwise_adamw_gb300 import workloads as W
     stream = torch.cuda.current_stream(device)
@@ -526,6 +532,16 @@ def run_secondary(args, wl8, states8, peak, device, world, barrier):
                      "achieved_gbs": gbs, "peak_gbs": peak, "frac": gbs / peak,
                      "algorithmic_bytes_per_launch": ab / nl,
                      "traffic": traffic_per_launch(kernel, wl.numel / nl) if nl == 1 else None}
+
+    # the headline step in the other mode, on the headline's state
+    other = 0 if args.exact else 1
+    packed8 = q8.pack_tensor8(states8)
+    per = _time_steps(lambda t: q8.adamw8bit_sr_step(packed8, q8.hparams(
+        lr=h8["lr"], beta1=h8["beta1"], beta2=h8["beta2"], eps=h8["eps"], weight_decay=h8["weight_decay"],
+        step=t, seed=wl8.philox_seed, exact=other), stream), args.secondary_steps, args.warmup, stream, device,
+        barrier)
+    entry("adamw8bit_exact" if other else "adamw8bit_fast", wl8, "step8_kernel", 2, per, launches_per_step(wl8))
+    del packed8
 
     # one-state steps on the 6.7B list: the m codes and absmax of the headline state
     one = [q8.Tensor8(s.param, s.grad, m_codes=s.m_codes, m_absmax=s.m_absmax) for s in states8]
@@ -550,7 +566,8 @@ def run_secondary(args, wl8, states8, peak, device, world, barrier):
     h16 = dict(wl16.hp)
     per = _time_steps(lambda t: q8.adamw_bf16_sr_step(packed16, q8.hparams(
         lr=h16["lr"], beta1=h16["beta1"], beta2=h16["beta2"], eps=h16["eps"], weight_decay=h16["weight_decay"],
-        step=t, seed=wl16.philox_seed), stream), args.secondary_steps, args.warmup, stream, device, barrier)
+        step=t, seed=wl16.philox_seed, exact=int(args.exact)), stream), args.secondary_steps, args.warmup, stream,
+        device, barrier)
     entry("adamw_bf16", wl16, "step16_kernel", 2, per, launches_per_step(wl16))
     del st16, packed16, p16, g16
     torch.cuda.empty_cache()

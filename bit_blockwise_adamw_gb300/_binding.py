@@ -41,7 +41,7 @@ class HParams(C.Structure):
     """q8_adamw_hparams."""
     _fields_ = [("lr", C.c_double), ("beta1", C.c_double), ("beta2", C.c_double),
                 ("eps", C.c_double), ("weight_decay", C.c_double),
-                ("step", C.c_int64), ("seed", C.c_uint64), ("sr", C.c_int32)]
+                ("step", C.c_int64), ("seed", C.c_uint64), ("sr", C.c_int32), ("exact", C.c_int32)]
 
 
 class MomentumHParams(C.Structure):
@@ -126,8 +126,10 @@ def _stream(stream):
     return C.c_void_p(int(stream))
 
 
-def hparams(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=1, seed=0, sr=1):
-    return HParams(lr, beta1, beta2, eps, weight_decay, step, seed, sr)
+def hparams(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=1, seed=0, sr=1, exact=0):
+    """q8_adamw_hparams; exact=0 is the fast mode (approximate square root and
+    reciprocal in the parameter update of full blocks), exact=1 the bit-exact one."""
+    return HParams(lr, beta1, beta2, eps, weight_decay, step, seed, sr, int(exact))
 
 
 def momentum_hparams(lr=1e-2, momentum=0.9, weight_decay=0.0, step=1, seed=0, sr=1):
@@ -185,9 +187,11 @@ def q8_philox_fill(seed: int, step: int, stream_id: int, offset: int, out: torch
 
 def q8_selftest_sqrt_div(counts: torch.Tensor, stream=None) -> None:
     """Device self-test of the packed square root and division; counts:
-    int64[6] on the GPU (reciprocal mismatches, d values checked, quotient
-    mismatches, pairs checked, square-root mismatches, v values checked)."""
-    assert counts.dtype == torch.int64 and counts.numel() >= 6 and counts.is_contiguous()
+    int64[8] on the GPU (reciprocal mismatches, d values checked, quotient
+    mismatches, pairs checked, square-root mismatches, v values checked, and
+    the largest relative errors of the fast mode's approximate square root and
+    reciprocal as float bit patterns)."""
+    assert counts.dtype == torch.int64 and counts.numel() >= 8 and counts.is_contiguous()
     _check("q8_selftest_sqrt_div", load_library().q8_selftest_sqrt_div(_ptr(counts), _stream(stream)))
 
 

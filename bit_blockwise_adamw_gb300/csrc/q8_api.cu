@@ -50,6 +50,7 @@ int make_scalars(const q8_adamw_hparams* hp, q8::Scalars* s)
     if (hp->weight_decay < 0.0) return fail(Q8_ERR_ARG, "weight_decay must be >= 0");
     if (hp->step < 1 || hp->step > Q8_MAX_STEP) return fail(Q8_ERR_ARG, "step must lie in [1, 2^31)");
     if (hp->sr != 0 && hp->sr != 1) return fail(Q8_ERR_ARG, "sr must be 0 or 1");
+    if (hp->exact != 0 && hp->exact != 1) return fail(Q8_ERR_ARG, "exact must be 0 or 1");
     const double t = static_cast<double>(hp->step);
     const double bc1 = 1.0 - std::pow(hp->beta1, t);
     const double bc2 = 1.0 - std::pow(hp->beta2, t);
@@ -64,6 +65,8 @@ int make_scalars(const q8_adamw_hparams* hp, q8::Scalars* s)
     s->key = q8::philox_key(hp->seed, static_cast<uint32_t>(hp->step));
     s->sr = hp->sr;
     s->fast_div = (s->eps_t >= 0x1p-100f && s->eps_t <= 0x1p20f) ? 1 : 0;
+    s->approx = (hp->exact == 0 && s->eps_t >= 0x1p-36f && s->eps_t <= 0x1p20f && s->step_size <= 1.0f) ? 1 : 0;
+    s->cancel = s->step_size * 0x1p-9f;
     return Q8_OK;
 }
 
@@ -201,7 +204,7 @@ void fill_common(q8::Scalars1& s, double lr, double wd, int64_t step, uint64_t s
 
 extern "C" {
 
-int q8_abi_version(void) { return 4; }
+int q8_abi_version(void) { return 5; }
 
 const char* q8_last_error(void) { return g_error.c_str(); }
 

@@ -217,6 +217,40 @@ __device__ __forceinline__ float2 ratio2_fast(const Scalars& s, float2 m, float2
     return div2_rn(m, __fadd2_rn(root, splat(s.eps_t)));
 }
 
+// The fast mode's m / (sqrt(v) + eps_t) of a pair: the hardware's approximate
+// square root and reciprocal (flush-to-zero forms, one instruction each, each
+// within 2^-21 relative error over every normal input, measured by
+// q8_selftest_sqrt_div), then one packed add and one packed multiply.  With
+// the roundings of the add and the multiply, the quotient q is within 2^-19
+// relative error of the correctly rounded one.  Callers use it when
+// Scalars::approx is set: eps_t in [2^-36, 2^20] keeps the denominator normal
+// and makes the square root of a subnormal v (flushed to 0) fall below half
+// an ulp of eps_t, as the exact step rounds it; infinite or NaN v gives 0 or
+// NaN as the division does.
+//
+// It feeds only the parameter update P = fma(-a_t, q, p*decay), never m or
+// v, so codes, absmax and BF16 moments are those of the exact step.  P itself
+// can move by a_t * 2^-19 * |q| plus its own rounding: when the update nearly
+// cancels p*decay that is many BF16 ulps of the small P.  So the callers redo
+// on the exact path every element unless |P| >= |q| * a_t * 2^-9
+// (Scalars::cancel; the AdamW kernel checks each element, the BF16-state
+// kernel the thread's smallest |P| against its largest |q|).  Past that bound
+// the two P lie fewer than 2^15 fp32 values apart, with the same sign, so
+// after the same 16-bit stochastic-rounding draw (or rounding to nearest
+// even) their BF16 results differ by one ulp at most.
+__device__ __forceinline__ float sqrt_approx(float v)
+{
+    float y;
+    asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(v));
+    return y;
+}
+
+__device__ __forceinline__ float2 ratio2_approx(const Scalars& s, float2 m, float2 v)
+{
+    const float2 den = __fadd2_rn(make_float2(sqrt_approx(v.x), sqrt_approx(v.y)), splat(s.eps_t));
+    return __fmul2_rn(m, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
+}
+
 // The parameter update of a pair given sqrt(v): p*decay - a_t*(m/(sqrt(v)+eps_t)).
 __device__ __forceinline__ float2 param2(const Scalars& s, float2 p, float2 m, float2 root)
 {

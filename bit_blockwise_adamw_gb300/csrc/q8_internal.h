@@ -66,6 +66,10 @@ struct Scalars {
     PhiloxKey key;
     int32_t sr;
     int32_t fast_div;          // eps_t in [2^-100, 2^20]: the packed division may be used
+    int32_t approx;            // the caller did not ask for exact, eps_t in [2^-36, 2^20] and
+                               // step_size <= 1: the full blocks' parameter update may use
+                               // the approximate square root and reciprocal (ratio2_approx)
+    float cancel;              // step_size * 2^-9: the cancellation bound of the fast mode
 };
 
 // Tensor lists travel as kernel parameters (no device allocation, no copy):

@@ -2,7 +2,10 @@
 // used by the AdamW steps (q8_device.cuh, "division"), against CUDA's IEEE
 // reciprocal, division and square root: every positive normal d with a normal
 // reciprocal for y = RN(1/d), seeded pseudo-random quotients inside the bounds
-// the steps check, and every normal v >= 2^-100 for the square root.
+// the steps check, and every normal v >= 2^-100 for the square root.  It also
+// measures the largest relative error of the approximate square root and
+// reciprocal of the fast mode (ratio2_approx), against double precision, over
+// every normal input.
 #include "q8_device.cuh"
 
 namespace q8 {
@@ -14,6 +17,7 @@ constexpr uint32_t kEndD = 0x7E800000u;        // 2^126: 1/d is normal below thi
 constexpr int kPairsPerD = 2;
 constexpr uint32_t kFirstV = 0x0D800000u;      // 2^-100
 constexpr uint32_t kEndV = 0x7F800000u;        // +inf
+constexpr uint32_t kFirstNormal = 0x00800000u; // 2^-126
 
 // A 32-bit integer mix (xor-shift-multiply) for the pseudo-random pairs.
 __device__ __forceinline__ uint32_t mix(uint32_t x)
@@ -60,10 +64,27 @@ __global__ void __launch_bounds__(256) selftest_kernel(unsigned long long* count
         const float2 r = sqrt2_rn(make_float2(v, v));
         bad_s += __float_as_uint(r.x) != __float_as_uint(__fsqrt_rn(v));
     }
+    // relative errors of the approximate square root (every normal v) and
+    // reciprocal (every normal d with a normal reciprocal), in double: the
+    // products below are exact in double, the square root correctly rounded
+    float err_s = 0.0f, err_r = 0.0f;
+    const uint32_t na = kEndV - kFirstNormal;
+    for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < na; i += gridDim.x * blockDim.x) {
+        const float v = __uint_as_float(kFirstNormal + i);
+        const double s = static_cast<double>(sqrt_approx(v));
+        err_s = fmaxf(err_s, static_cast<float>(fabs(s / sqrt(static_cast<double>(v)) - 1.0)));
+        if (kFirstNormal + i < kEndD) {
+            const double y = static_cast<double>(rcp_approx(v));
+            err_r = fmaxf(err_r, static_cast<float>(fabs(y * static_cast<double>(v) - 1.0)));
+        }
+    }
     atomicAdd(&counts[0], bad_y);
     atomicAdd(&counts[2], bad_q);
     atomicAdd(&counts[3], pairs);
     atomicAdd(&counts[4], bad_s);
+    // non-negative floats order like their bit patterns
+    atomicMax(&counts[6], static_cast<unsigned long long>(__float_as_uint(err_s)));
+    atomicMax(&counts[7], static_cast<unsigned long long>(__float_as_uint(err_r)));
     if (blockIdx.x == 0 && threadIdx.x == 0) {
         atomicAdd(&counts[1], static_cast<unsigned long long>(n));
         atomicAdd(&counts[5], static_cast<unsigned long long>(nv));
@@ -74,7 +95,7 @@ __global__ void __launch_bounds__(256) selftest_kernel(unsigned long long* count
 
 cudaError_t launch_selftest_sqrt_div(uint64_t* counts, cudaStream_t st)
 {
-    const cudaError_t e = cudaMemsetAsync(counts, 0, 6 * sizeof(uint64_t), st);
+    const cudaError_t e = cudaMemsetAsync(counts, 0, 8 * sizeof(uint64_t), st);
     if (e != cudaSuccess) return e;
     int grid = 0;
     const cudaError_t eg = persistent_grid(reinterpret_cast<const void*>(selftest_kernel), 256, 0, &grid);

@@ -49,8 +49,10 @@ __device__ __forceinline__ void store8_bf16(uint16_t* dst, int64_t rem, const ui
 }
 
 // One 2048-element block: FULL blocks lie wholly inside the tensor (vector
-// loads and stores only); otherwise the partial last block.
-template <bool SR, bool FULL>
+// loads and stores only); otherwise the partial last block.  APPROX (full
+// blocks only): the parameter update takes the approximate square root and
+// reciprocal (ratio2_approx); m and v never depend on them.
+template <bool SR, bool FULL, bool APPROX = false>
 __device__ __forceinline__ void block16(const Scalars& s, const Desc16& d, int lb)
 {
     const int64_t i0 = static_cast<int64_t>(lb) * kBlock + threadIdx.x * kVec;
@@ -88,24 +90,41 @@ __device__ __forceinline__ void block16(const Scalars& s, const Desc16& d, int l
         v[k] = bf16x2(vw[k]);
         moments2(s, bf16x2(gw[k]), m[k], v[k]);
     }
-    // the packed square root and division where they are exact (bounds in
+    // fast mode: the approximate quotient with the thread's cancellation
+    // check (ratio2_approx); otherwise, or to redo the thread, the packed
+    // square root and division where they are exact (bounds in
     // q8_device.cuh); padding elements of a ragged tail are zero and send
     // that thread to the IEEE path
-    const float lo = fminf(min3(fabsf(m[0].x), fabsf(m[0].y), fabsf(m[1].x)),
-                           min3(fabsf(m[1].y), fabsf(m[2].x), fminf(fabsf(m[2].y), fminf(fabsf(m[3].x), fabsf(m[3].y)))));
-    const float hi = fmaxf(max3(fabsf(m[0].x), fabsf(m[0].y), fabsf(m[1].x)),
-                           max3(fabsf(m[1].y), fabsf(m[2].x), fmaxf(fabsf(m[2].y), fmaxf(fabsf(m[3].x), fabsf(m[3].y)))));
-    const float vlo = fminf(min3(v[0].x, v[0].y, v[1].x), min3(v[1].y, v[2].x, fminf(v[2].y, fminf(v[3].x, v[3].y))));
-    const float vhi = fmaxf(max3(v[0].x, v[0].y, v[1].x), max3(v[1].y, v[2].x, fmaxf(v[2].y, fmaxf(v[3].x, v[3].y))));
-    if (s.fast_div && lo >= kDivMinM && hi <= kDivMaxM && vlo >= kSqrtMinV && vhi <= kDivMaxV) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k)
-            po[k] = round2<SR>(step2(s, bf16x2(pw[k]), ratio2_fast(s, m[k], sqrt2_rn(v[k]))), rp[k]);
-    } else {
+    bool redo = true;
+    if constexpr (FULL && APPROX) {
+        float qmax = 0.0f, pmin = __uint_as_float(0x7F800000u);
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const float2 root = make_float2(__fsqrt_rn(v[k].x), __fsqrt_rn(v[k].y));
-            po[k] = round2<SR>(param2(s, bf16x2(pw[k]), m[k], root), rp[k]);
+            const float2 q = ratio2_approx(s, m[k], v[k]);
+            const float2 x = step2(s, bf16x2(pw[k]), q);
+            qmax = max3(qmax, fabsf(q.x), fabsf(q.y));
+            pmin = min3(pmin, fabsf(x.x), fabsf(x.y));
+            po[k] = round2<SR>(x, rp[k]);
+        }
+        redo = pmin < qmax * s.cancel;
+    }
+    if (redo) {
+        const float lo = fminf(min3(fabsf(m[0].x), fabsf(m[0].y), fabsf(m[1].x)),
+                               min3(fabsf(m[1].y), fabsf(m[2].x), fminf(fabsf(m[2].y), fminf(fabsf(m[3].x), fabsf(m[3].y)))));
+        const float hi = fmaxf(max3(fabsf(m[0].x), fabsf(m[0].y), fabsf(m[1].x)),
+                               max3(fabsf(m[1].y), fabsf(m[2].x), fmaxf(fabsf(m[2].y), fmaxf(fabsf(m[3].x), fabsf(m[3].y)))));
+        const float vlo = fminf(min3(v[0].x, v[0].y, v[1].x), min3(v[1].y, v[2].x, fminf(v[2].y, fminf(v[3].x, v[3].y))));
+        const float vhi = fmaxf(max3(v[0].x, v[0].y, v[1].x), max3(v[1].y, v[2].x, fmaxf(v[2].y, fmaxf(v[3].x, v[3].y))));
+        if (s.fast_div && lo >= kDivMinM && hi <= kDivMaxM && vlo >= kSqrtMinV && vhi <= kDivMaxV) {
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                po[k] = round2<SR>(step2(s, bf16x2(pw[k]), ratio2_fast(s, m[k], sqrt2_rn(v[k]))), rp[k]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 root = make_float2(__fsqrt_rn(v[k].x), __fsqrt_rn(v[k].y));
+                po[k] = round2<SR>(param2(s, bf16x2(pw[k]), m[k], root), rp[k]);
+            }
         }
     }
 #pragma unroll
@@ -124,7 +143,7 @@ __device__ __forceinline__ void block16(const Scalars& s, const Desc16& d, int l
     }
 }
 
-template <bool SR>
+template <bool SR, bool APPROX>
 __global__ void __launch_bounds__(kThreads, 4) step16_kernel(const __grid_constant__ Step16Args a)
 {
     const int begin = static_cast<int>((static_cast<int64_t>(blockIdx.x) * a.nblocks) / gridDim.x);
@@ -137,7 +156,7 @@ __global__ void __launch_bounds__(kThreads, 4) step16_kernel(const __grid_consta
         const int base = a.blk_start[ti];
         const int stop = min(end, a.blk_start[ti + 1]);
         const int full_end = min(stop, base + static_cast<int>(d.n / kBlock));
-        for (; gb < full_end; ++gb) block16<SR, true>(a.s, d, gb - base);
+        for (; gb < full_end; ++gb) block16<SR, true, APPROX>(a.s, d, gb - base);
         for (; gb < stop; ++gb) block16<SR, false>(a.s, d, gb - base);
     }
 }
@@ -147,24 +166,36 @@ __global__ void __launch_bounds__(kThreads, 4) step16_kernel(const __grid_consta
 cudaError_t prepare_step16()
 {
     int g = 0;
-    cudaError_t e = persistent_grid(reinterpret_cast<const void*>(step16_kernel<true>), kThreads, 0, &g);
-    if (e == cudaSuccess) e = persistent_grid(reinterpret_cast<const void*>(step16_kernel<false>), kThreads, 0, &g);
-    return e;
+    const void* ks[] = {reinterpret_cast<const void*>(step16_kernel<true, true>),
+                        reinterpret_cast<const void*>(step16_kernel<true, false>),
+                        reinterpret_cast<const void*>(step16_kernel<false, true>),
+                        reinterpret_cast<const void*>(step16_kernel<false, false>)};
+    for (const void* k : ks) {
+        const cudaError_t e = persistent_grid(k, kThreads, 0, &g);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
+
+namespace {
+
+template <bool SR, bool APPROX>
+cudaError_t launch16_t(const Step16Args& a, cudaStream_t st)
+{
+    int full = 0;
+    const cudaError_t e = persistent_grid(reinterpret_cast<const void*>(step16_kernel<SR, APPROX>), kThreads, 0, &full);
+    if (e != cudaSuccess) return e;
+    const int grid = a.nblocks < full ? a.nblocks : full;
+    if (grid > 0) step16_kernel<SR, APPROX><<<grid, kThreads, 0, st>>>(a);
+    return cudaGetLastError();
+}
+
+}  // namespace
 
 cudaError_t launch_step16(const Step16Args& a, cudaStream_t st)
 {
-    const void* k = a.s.sr ? reinterpret_cast<const void*>(step16_kernel<true>)
-                           : reinterpret_cast<const void*>(step16_kernel<false>);
-    int full = 0;
-    const cudaError_t e = persistent_grid(k, kThreads, 0, &full);
-    if (e != cudaSuccess) return e;
-    const int grid = a.nblocks < full ? a.nblocks : full;
-    if (grid > 0) {
-        if (a.s.sr) step16_kernel<true><<<grid, kThreads, 0, st>>>(a);
-        else step16_kernel<false><<<grid, kThreads, 0, st>>>(a);
-    }
-    return cudaGetLastError();
+    if (a.s.sr) return a.s.approx ? launch16_t<true, true>(a, st) : launch16_t<true, false>(a, st);
+    return a.s.approx ? launch16_t<false, true>(a, st) : launch16_t<false, false>(a, st);
 }
 
 }  // namespace q8

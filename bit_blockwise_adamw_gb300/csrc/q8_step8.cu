@@ -17,7 +17,8 @@
 // allow it, else two 16-byte loads) and of both code arrays.  The kernel is
 // bound by instruction issue rather than by DRAM, so the loop is written to
 // keep the instruction count down: packed fp32x2 arithmetic (with a packed
-// exact square root and division wherever a thread's values allow it),
+// exact square root and division wherever a thread's values allow it, or in
+// the fast mode the hardware's approximate ones under a cancellation check),
 // codebook lookups whose address is one byte permute and that never share a
 // shared-memory bank within a warp, one lookup per code in the search, warp
 // reductions with redux.sync.
@@ -203,6 +204,9 @@ struct Prefetch {
 // valid elements (the hot path: vector loads and stores only, lane-replicated
 // codebooks); otherwise the block is the partial last block of its tensor.
 // W32: grad and param move in 32-byte accesses (all 32-byte aligned).
+// APPROX (full blocks only): the fast mode; the parameter update takes the
+// approximate square root and reciprocal (ratio2_approx) instead of the exact
+// ones, with its element-by-element cancellation check.
 // `it` picks the half of the double-buffered reduction scratch.
 // 32-byte streaming load and store (sixteen bf16 values), for launches whose
 // grad and param arrays are all 32-byte aligned: one instruction where two
@@ -220,7 +224,7 @@ __device__ __forceinline__ void st32(void* p, const uint32_t (&w)[8])
                  : "memory");
 }
 
-template <bool SR, bool FULL, bool W32 = false>
+template <bool SR, bool FULL, bool W32 = false, bool APPROX = false>
 __device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int lb, int it, const Smem8& sm,
                                            const Prefetch& pf, int tid, int bar, int lead)
 {
@@ -305,22 +309,51 @@ __device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int
                            fmaxf(absmax4(m[4], m[5]), absmax4(m[6], m[7])));
     const float lv = fmaxf(fmaxf(absmax4(v[0], v[1]), absmax4(v[2], v[3])),
                            fmaxf(absmax4(v[4], v[5]), absmax4(v[6], v[7])));
-    bool fast = false;
-    if constexpr (FULL) {
-        const float lo = fminf(fminf(absmin4(m[0], m[1]), absmin4(m[2], m[3])),
-                               fminf(absmin4(m[4], m[5]), absmin4(m[6], m[7])));
-        const float lov = fminf(fminf(min4(v[0], v[1]), min4(v[2], v[3])), fminf(min4(v[4], v[5]), min4(v[6], v[7])));
-        fast = s.fast_div && lo >= kDivMinM && lm <= kDivMaxM && lv <= kDivMaxV && lov >= kSqrtMinV;
-    }
-    if (fast) {
+    if constexpr (FULL && APPROX) {
+        // fast mode: the approximate quotient (ratio2_approx), checked for
+        // cancellation element by element, two pairs to a branch; pairs that
+        // fail take the IEEE square root and division
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
-            po[k] = round2<SR>(step2(s, bf16x2(f.p[k]), ratio2_fast(s, m[k], sqrt2_rn(v[k]))), r[k]);
+        for (int k0 = 0; k0 < 8; k0 += 2) {
+            float2 x[2];
+            bool redo = false;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const float2 q = ratio2_approx(s, m[k0 + j], v[k0 + j]);
+                x[j] = step2(s, bf16x2(f.p[k0 + j]), q);
+                const float2 t = __fmul2_rn(q, splat(s.cancel));
+                redo = redo | (fabsf(x[j].x) < fabsf(t.x)) | (fabsf(x[j].y) < fabsf(t.y));
+            }
+            if (redo) {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                    const int k = k0 + j;
+                    const float2 root = make_float2(__fsqrt_rn(v[k].x), __fsqrt_rn(v[k].y));
+                    x[j] = param2(s, bf16x2(f.p[k]), m[k], root);
+                }
+            }
+#pragma unroll
+            for (int j = 0; j < 2; ++j) po[k0 + j] = round2<SR>(x[j], r[k0 + j]);
+        }
     } else {
+        bool fast = false;
+        if constexpr (FULL) {
+            const float lo = fminf(fminf(absmin4(m[0], m[1]), absmin4(m[2], m[3])),
+                                   fminf(absmin4(m[4], m[5]), absmin4(m[6], m[7])));
+            const float lov = fminf(fminf(min4(v[0], v[1]), min4(v[2], v[3])),
+                                    fminf(min4(v[4], v[5]), min4(v[6], v[7])));
+            fast = s.fast_div && lo >= kDivMinM && lm <= kDivMaxM && lv <= kDivMaxV && lov >= kSqrtMinV;
+        }
+        if (fast) {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) {
-            const float2 root = make_float2(__fsqrt_rn(v[k].x), __fsqrt_rn(v[k].y));
-            po[k] = round2<SR>(param2(s, bf16x2(f.p[k]), m[k], root), r[k]);
+            for (int k = 0; k < 8; ++k)
+                po[k] = round2<SR>(step2(s, bf16x2(f.p[k]), ratio2_fast(s, m[k], sqrt2_rn(v[k]))), r[k]);
+        } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const float2 root = make_float2(__fsqrt_rn(v[k].x), __fsqrt_rn(v[k].y));
+                po[k] = round2<SR>(param2(s, bf16x2(f.p[k]), m[k], root), r[k]);
+            }
         }
     }
 
@@ -381,7 +414,7 @@ __device__ __forceinline__ bool is_partial(const Desc8& d, int lb)
 // are left to step8_tail_kernel, so this loop carries no ragged-tail code.
 // Each group of each CTA takes a contiguous range of the list's blocks (end to
 // end over the tensors).
-template <bool SR, bool W32>
+template <bool SR, bool W32, bool APPROX>
 __global__ void __launch_bounds__(kT8 * kGroups, 1) step8_kernel(const __grid_constant__ Step8Args a)
 {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -419,7 +452,7 @@ __global__ void __launch_bounds__(kT8 * kGroups, 1) step8_kernel(const __grid_co
         const int next = a.blk_start[ti + 1];
         const int full_end = min(min(end, next), base + static_cast<int>(d.n / kBlock));
         for (; gb < full_end; ++gb)
-            block_step<SR, true, W32>(a.s, d, gb - base, it++, sm, Prefetch{&a, gb + kAhead, next, base, ti, gb + kAhead < end},
+            block_step<SR, true, W32, APPROX>(a.s, d, gb - base, it++, sm, Prefetch{&a, gb + kAhead, next, base, ti, gb + kAhead < end},
                                  tid, 1 + grp, lead);
         gb = min(end, next);                             // a partial last block is the tail kernel's
     }
@@ -473,15 +506,16 @@ __global__ void __launch_bounds__(kSmallThreads) step32_kernel(const __grid_cons
     }
 }
 
-template <bool SR, bool W32>
+template <bool SR, bool W32, bool APPROX>
 cudaError_t launch_step8_t(const Step8Args& a, bool has_partial, cudaStream_t st)
 {
     int full = 0, unused = 0;
-    cudaError_t e = persistent_grid(reinterpret_cast<const void*>(step8_kernel<SR, W32>), kT8 * kGroups, kSmemBytes, &full);
+    cudaError_t e = persistent_grid(reinterpret_cast<const void*>(step8_kernel<SR, W32, APPROX>), kT8 * kGroups,
+                                    kSmemBytes, &full);
     if (e != cudaSuccess) return e;
     const int per = (a.nblocks + kGroups - 1) / kGroups;
     const int grid = per < full ? per : full;
-    if (grid > 0) step8_kernel<SR, W32><<<grid, kT8 * kGroups, kSmemBytes, st>>>(a);
+    if (grid > 0) step8_kernel<SR, W32, APPROX><<<grid, kT8 * kGroups, kSmemBytes, st>>>(a);
     if (has_partial && a.nt > 0) {
         e = persistent_grid(reinterpret_cast<const void*>(step8_tail_kernel<SR>), kT8, kTailSmemBytes, &unused);
         if (e != cudaSuccess) return e;
@@ -495,8 +529,14 @@ cudaError_t launch_step8_t(const Step8Args& a, bool has_partial, cudaStream_t st
 cudaError_t prepare_step8()
 {
     int g = 0;
-    const void* ks[] = {reinterpret_cast<const void*>(step8_kernel<true, true>), reinterpret_cast<const void*>(step8_kernel<true, false>),
-                        reinterpret_cast<const void*>(step8_kernel<false, true>), reinterpret_cast<const void*>(step8_kernel<false, false>)};
+    const void* ks[] = {reinterpret_cast<const void*>(step8_kernel<true, true, true>),
+                        reinterpret_cast<const void*>(step8_kernel<true, true, false>),
+                        reinterpret_cast<const void*>(step8_kernel<true, false, true>),
+                        reinterpret_cast<const void*>(step8_kernel<true, false, false>),
+                        reinterpret_cast<const void*>(step8_kernel<false, true, true>),
+                        reinterpret_cast<const void*>(step8_kernel<false, true, false>),
+                        reinterpret_cast<const void*>(step8_kernel<false, false, true>),
+                        reinterpret_cast<const void*>(step8_kernel<false, false, false>)};
     const void* ts[] = {reinterpret_cast<const void*>(step8_tail_kernel<true>),
                         reinterpret_cast<const void*>(step8_tail_kernel<false>)};
     for (const void* k : ks) {
@@ -519,8 +559,13 @@ cudaError_t launch_step8(const Step8Args& a, cudaStream_t st)
     bool w32 = true;
     for (int i = 0; i < a.nt; ++i)
         w32 = w32 && (reinterpret_cast<uintptr_t>(a.d[i].g) % 32) == 0 && (reinterpret_cast<uintptr_t>(a.d[i].p) % 32) == 0;
-    if (a.s.sr) return w32 ? launch_step8_t<true, true>(a, has_partial, st) : launch_step8_t<true, false>(a, has_partial, st);
-    return w32 ? launch_step8_t<false, true>(a, has_partial, st) : launch_step8_t<false, false>(a, has_partial, st);
+    const bool ax = a.s.approx != 0;
+    if (a.s.sr) {
+        if (w32) return ax ? launch_step8_t<true, true, true>(a, has_partial, st) : launch_step8_t<true, true, false>(a, has_partial, st);
+        return ax ? launch_step8_t<true, false, true>(a, has_partial, st) : launch_step8_t<true, false, false>(a, has_partial, st);
+    }
+    if (w32) return ax ? launch_step8_t<false, true, true>(a, has_partial, st) : launch_step8_t<false, true, false>(a, has_partial, st);
+    return ax ? launch_step8_t<false, false, true>(a, has_partial, st) : launch_step8_t<false, false, false>(a, has_partial, st);
 }
 
 cudaError_t launch_step32(const Step32Args& a, cudaStream_t st)

@@ -137,18 +137,21 @@ class _Q8Optimizer(_FrontEnd):
 
 class AdamW8bitSR(_Q8Optimizer):
     """AdamW with 8-bit blockwise m, v and stochastically rounded bf16 params
-    (adamw8bit_sr_step).  Parameters below 4096 elements keep fp32 state."""
+    (adamw8bit_sr_step).  Parameters below 4096 elements keep fp32 state.
+    exact=True asks for the bit-exact mode (correctly rounded square root and
+    division); the default fast mode differs from it by at most one bf16 ulp
+    on rare parameters, never in the state."""
 
     def __init__(self, params, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=1e-2, seed=0,
-                 stochastic_rounding=True):
+                 stochastic_rounding=True, exact=False):
         super().__init__(params, dict(lr=lr, betas=betas, eps=eps, weight_decay=weight_decay, seed=seed,
-                                      sr=int(stochastic_rounding)))
+                                      sr=int(stochastic_rounding), exact=int(exact)))
 
     def _run(self, group, arr):
         b1, b2 = group["betas"]
         B.adamw8bit_sr_step(arr, B.hparams(lr=group["lr"], beta1=b1, beta2=b2, eps=group["eps"],
                                            weight_decay=group["weight_decay"], step=group["step"],
-                                           seed=group["seed"], sr=group["sr"]))
+                                           seed=group["seed"], sr=group["sr"], exact=group.get("exact", 0)))
 
 
 class Momentum8bitSR(_Q8Optimizer):
@@ -186,9 +189,9 @@ class AdamWBF16SR(_FrontEnd):
     _struct = (B._Tensor16, _T16_FIELDS)
 
     def __init__(self, params, lr=1e-3, betas=(0.9, 0.999), eps=1e-8, weight_decay=1e-2, seed=0,
-                 stochastic_rounding=True):
+                 stochastic_rounding=True, exact=False):
         super().__init__(params, dict(lr=lr, betas=betas, eps=eps, weight_decay=weight_decay, seed=seed,
-                                      sr=int(stochastic_rounding)))
+                                      sr=int(stochastic_rounding), exact=int(exact)))
 
     def _row(self, p):
         _check_param(p)
@@ -204,4 +207,4 @@ class AdamWBF16SR(_FrontEnd):
         b1, b2 = group["betas"]
         B.adamw_bf16_sr_step(arr, B.hparams(lr=group["lr"], beta1=b1, beta2=b2, eps=group["eps"],
                                             weight_decay=group["weight_decay"], step=group["step"],
-                                            seed=group["seed"], sr=group["sr"]))
+                                            seed=group["seed"], sr=group["sr"], exact=group.get("exact", 0)))

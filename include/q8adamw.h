@@ -73,12 +73,23 @@ enum {
  *   m = fma(beta1, m, (1-beta1)*g);  v = fma(beta2, v, (1-beta2)*(g*g));
  *   p = fma(-a_t, m / (sqrt(v) + eps_t), p*decay)
  * which is textbook AdamW with decoupled weight decay ([LLM] TL;DR).
+ * exact = 1 takes the square root and the division correctly rounded
+ * everywhere, so that every output is bit-identical with the plain CPU
+ * restatement of these formulas.  exact = 0 (the fast mode) lets the full
+ * 2048-blocks of the 8-bit and BF16-state kernels take them from the
+ * hardware's approximate square root and reciprocal (when eps_t lies in
+ * [2^-100, 2^20]; otherwise exact).  Both feed only the parameter update, so
+ * codes, absmax and the BF16 m and v are identical in both modes; a parameter
+ * differs only where the approximation moves its BF16 rounding, by one ulp
+ * on a few elements in a million per step.
+ * Any other value of sr or exact is an argument error.
  */
 typedef struct {
     double lr, beta1, beta2, eps, weight_decay;
     int64_t step;
     uint64_t seed;
     int32_t sr;
+    int32_t exact;
 } q8_adamw_hparams;
 
 /*
@@ -244,9 +255,14 @@ int q8_philox_fill(uint64_t seed, uint32_t step, uint32_t stream_id, uint64_t of
  *               which the steps use it (2^-90 <= |m| <= 2^26,
  *               2^-100 <= d <= 2^21), both signs of m;
  *   counts[4] = v values whose square root differs from __fsqrt_rn(v), over
- *               every normal v >= 2^-100 (counts[5] of them).
- * counts: device uint64[6] (8-byte aligned), overwritten.  Takes about a
- * second on one GPU.
+ *               every normal v >= 2^-100 (counts[5] of them);
+ *   counts[6] = the largest relative error of the approximate square root of
+ *               the fast mode (sqrt.approx.ftz.f32) over every normal v, and
+ *   counts[7] = that of its approximate reciprocal (rcp.approx.ftz.f32) over
+ *               every normal d with a normal reciprocal, each the bit pattern
+ *               of a float (errors measured in double precision).
+ * counts: device uint64[8] (8-byte aligned), overwritten.  Takes a few
+ * seconds on one GPU.
  */
 int q8_selftest_sqrt_div(uint64_t* counts, q8_stream_t stream);
 
@@ -264,7 +280,7 @@ int q8_prepare_device(void);
 const char* q8_last_error(void);
 
 /* ABI version: bumped on any change of a signature or struct. */
-int q8_abi_version(void);   /* 4 */
+int q8_abi_version(void);   /* 5 */
 
 #ifdef __cplusplus
 }

@@ -45,9 +45,60 @@ def host_states8(params_host, offsets=None):
             for p, off in zip(params_host, offsets)]
 
 
-def compare_state8(gpu, host, where=""):
-    """Bit-exact comparison of one tensor's parameters and state."""
-    np.testing.assert_array_equal(u16(gpu.param), host.param, err_msg="param " + where)
+# The fast mode (exact=0: approximate square root and reciprocal in the
+# parameter update) against the oracle, at the tolerance the target states
+# for floating-point results: BF16 parameters bit-exact on at least 99.9 % of
+# elements and within one BF16 ulp on the rest, for a step from identical
+# inputs.  Codes, absmax, fp32 state and BF16 moments do not depend on the
+# approximation and stay bit-exact.  Along a whole run a parameter that once
+# differed by an ulp keeps that small absolute offset, which a later update
+# that nearly cancels it can make many ulps of the small result; whole runs
+# are therefore held to the share alone (ParamTolerance(ulps=None)).
+PARAM_EXACT_SHARE = 0.999
+
+
+def bf16_ulps(a, b):
+    """Distance between arrays of BF16 bit patterns in units in the last
+    place, along the ordered line of BF16 values (+0 and -0 coincide)."""
+    def key(x):
+        x = np.asarray(x).astype(np.int32)
+        return np.where(x & 0x8000, -(x & 0x7FFF), x)
+    return np.abs(key(a) - key(b))
+
+
+class ParamTolerance:
+    """Tally of the BF16 parameters compared in the fast mode: every one within
+    `ulps` of the oracle's (no bound for ulps=None), and (check()) at most
+    0.1 % of them different."""
+
+    def __init__(self, ulps=1):
+        self.ulps = ulps
+        self.n = 0
+        self.diff = 0
+        self.max_ulps = 0
+
+    def add(self, got, want, where=""):
+        d = bf16_ulps(got, want)
+        self.n += d.size
+        self.diff += int(np.count_nonzero(d))
+        if d.size:
+            worst = int(d.max())
+            self.max_ulps = max(self.max_ulps, worst)
+            assert self.ulps is None or worst <= self.ulps, \
+                "param %s: %d ulps from the oracle at %d" % (where, worst, int(d.argmax()))
+
+    def check(self):
+        assert self.diff <= (1.0 - PARAM_EXACT_SHARE) * self.n, \
+            "%d of %d parameters differ from the oracle" % (self.diff, self.n)
+
+
+def compare_state8(gpu, host, where="", tol=None):
+    """Comparison of one tensor's parameters and state: bit-exact, or with
+    the parameters tallied in `tol` (a ParamTolerance) for the fast mode."""
+    if tol is None:
+        np.testing.assert_array_equal(u16(gpu.param), host.param, err_msg="param " + where)
+    else:
+        tol.add(u16(gpu.param), host.param, where)
     if host.m_codes is not None:
         np.testing.assert_array_equal(gpu.m_codes.cpu().numpy(), host.m_codes, err_msg="m codes " + where)
         np.testing.assert_array_equal(gpu.v_codes.cpu().numpy(), host.v_codes, err_msg="v codes " + where)
@@ -169,8 +220,10 @@ class SampledRun:
     """Run a full-size workload on the GPU while recording the inputs of the
     sampled blocks (and of every small tensor) for an oracle replay."""
 
-    def __init__(self, wl, device, fraction, steps=None, extra_blocks=(), opt=None):
+    def __init__(self, wl, device, fraction, steps=None, extra_blocks=(), opt=None, exact=True):
         self.wl = wl
+        self.exact = exact              # AdamW: the bit-exact mode, or the fast one
+        self.tol = None
         self.opt = opt                  # None: AdamW; o.MOMENTUM or o.LION: the one-state step
         self.steps = steps or wl.steps
         self.device = device
@@ -232,9 +285,9 @@ class SampledRun:
                     lr=h["lr"], beta1=h["beta1"], beta2=h["beta2"], weight_decay=h["weight_decay"], step=step,
                     seed=h["seed"]))
             elif wl.state == "8bit":
-                q8.adamw8bit_sr_step(packed, q8.hparams(**h))
+                q8.adamw8bit_sr_step(packed, q8.hparams(**h, exact=int(self.exact)))
             else:
-                q8.adamw_bf16_sr_step(packed, q8.hparams(**h))
+                q8.adamw_bf16_sr_step(packed, q8.hparams(**h, exact=int(self.exact)))
             self.grads.append(self._slices(grads))
             self.hps.append(h)
             del grads
@@ -292,6 +345,7 @@ class SampledRun:
                 fns.append(_replay16)
         results = [pool.apply_async(f, (job,)) for f, (_, job) in zip(fns, jobs)]
         compared = 0
+        tol = None if self.exact or self.opt is not None else ParamTolerance(ulps=None)
         for (k, _), r in zip(jobs, results):
             want = r.get()
             got = self.final[k]
@@ -299,6 +353,9 @@ class SampledRun:
             for name, gv, wv in zip(names, got, want):
                 gv = np.asarray(gv)
                 wv = np.asarray(wv)
+                if tol is not None and name == "param":
+                    tol.add(gv, wv, "tensor %d block %d" % k)
+                    continue
                 if gv.dtype == np.float32:
                     gv, wv = gv.view(np.uint32), wv.view(np.uint32)
                 if not np.array_equal(gv, wv):
@@ -307,4 +364,7 @@ class SampledRun:
                                          "(gpu %r oracle %r)" % (name, k[0], k[1], bad.size, gv.size,
                                                                   bad[0], gv[bad[0]], wv[bad[0]]))
             compared += got[0].size
+        if tol is not None:
+            tol.check()
+            self.tol = tol
         return compared

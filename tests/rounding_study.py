@@ -154,7 +154,7 @@ def run(regime, seed, steps, device, every=None):
         host_g.numpy()[:] = gb.view(np.int16)
         grad.view(torch.int16).copy_(host_g)
         for name, sr in ROUNDINGS.items():
-            hp = q8.hparams(lr=cfg["lr"], beta1=B1, beta2=B2, eps=EPS, weight_decay=cfg["wd"],
+            hp = q8.hparams(exact=1, lr=cfg["lr"], beta1=B1, beta2=B2, eps=EPS, weight_decay=cfg["wd"],
                             step=t, seed=seed, sr=sr)
             q8.adamw8bit_sr_step(lists8[name], hp)
             q8.adamw_bf16_sr_step(lists16[name], hp)

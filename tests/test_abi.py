@@ -40,7 +40,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 
 def test_abi_version(lib):
-    assert q8.q8_abi_version() == 4
+    assert q8.q8_abi_version() == 5
 
 
 @pytest.mark.parametrize("kind", [q8.SIGNED, q8.UNSIGNED])
@@ -81,7 +81,7 @@ def test_state_picks_the_path(lib):
 
 @pytest.mark.parametrize("field,value", [
     ("step", 0), ("step", 1 << 31), ("beta1", 1.0), ("beta2", -0.1), ("lr", float("nan")),
-    ("eps", -1.0), ("weight_decay", float("inf")), ("sr", 2)])
+    ("eps", -1.0), ("weight_decay", float("inf")), ("sr", 2), ("exact", 2), ("exact", -1)])
 def test_step8_rejects_bad_hparams(lib, field, value):
     hp = q8.hparams()
     setattr(hp, field, value)

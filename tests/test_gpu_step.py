@@ -15,8 +15,8 @@ import bit_blockwise_adamw_gb300 as q8
 from bit_blockwise_adamw_gb300 import workloads as W
 import oracle as o
 
-from parity import (SampledRun, compare_slice8, compare_state8, gpu_states8, host_slice8, host_states8, hp_for,
-                    oracle_pool, shift16, u16)
+from parity import (ParamTolerance, SampledRun, compare_slice8, compare_state8, gpu_states8, host_slice8,
+                    host_states8, hp_for, oracle_pool, shift16, u16)
 
 pytestmark = pytest.mark.gpu
 
@@ -29,11 +29,15 @@ def pool():
     p.join()
 
 
-def _run_full(wl, device, steps=None, sr=1, offsets=None, split=None, grad_hook=None, param_hook=None, shifted=()):
+def _run_full(wl, device, steps=None, sr=1, offsets=None, split=None, grad_hook=None, param_hook=None, shifted=(),
+              exact=True):
     """Run `wl` on both sides for `steps`, comparing everything after each step
     (`grad_hook(step, grads)` may edit the step's gradients in place first,
     `param_hook(params)` the initial parameters; the params and grads of the
-    tensors in `shifted` sit 16 bytes past a 32-byte boundary)."""
+    tensors in `shifted` sit 16 bytes past a 32-byte boundary).  exact=False
+    runs the fast mode and holds the parameters of each step to its tolerance,
+    then gives the GPU the oracle's parameters, so that every step starts from
+    identical inputs."""
     steps = steps or wl.steps
     params = W.init_params(wl, device)
     params = [shift16(p) if i in shifted else p for i, p in enumerate(params)]
@@ -51,34 +55,48 @@ def _run_full(wl, device, steps=None, sr=1, offsets=None, split=None, grad_hook=
             g_host.grad = u16(gr)
         h = hp_for(wl, step, sr)
         if split:
-            q8.adamw8bit_sr_step(gpu[:split], q8.hparams(**h))
-            q8.adamw8bit_sr_step(gpu[split:], q8.hparams(**h))
+            q8.adamw8bit_sr_step(gpu[:split], q8.hparams(**h, exact=int(exact)))
+            q8.adamw8bit_sr_step(gpu[split:], q8.hparams(**h, exact=int(exact)))
         else:
-            q8.adamw8bit_sr_step(gpu, q8.hparams(**h))
+            q8.adamw8bit_sr_step(gpu, q8.hparams(**h, exact=int(exact)))
         o.adamw8bit_sr_step(host, o.hparams(**h))
         torch.cuda.synchronize()
+        tol = None if exact else ParamTolerance()
         for i, (a, b) in enumerate(zip(gpu, host)):
-            compare_state8(a, b, "tensor %d step %d" % (i, step))
+            compare_state8(a, b, "tensor %d step %d" % (i, step), tol)
+        if tol is not None:
+            tol.check()
+            for a, b in zip(gpu, host):             # identical inputs for the next step
+                a.param.copy_(torch.from_numpy(b.param.view(np.int16)).view(torch.bfloat16).to(a.param.device))
     return gpu, host
 
 
-def test_flat_1m_full_parity(cuda_device):
-    """1,048,576 params, 512 blocks, 10 steps, every element every step."""
-    _run_full(W.WORKLOADS["flat-1m"], cuda_device)
+MODES = [True, False]
+MODE_IDS = ["exact", "fast"]
+
+
+@pytest.mark.parametrize("exact", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("sr", [1, 0])
+def test_flat_1m_full_parity(cuda_device, sr, exact):
+    """1,048,576 params, 512 blocks, 10 steps, every element every step, in
+    the bit-exact and the fast mode."""
+    _run_full(W.WORKLOADS["flat-1m"], cuda_device, sr=sr, exact=exact)
 
 
 EDGE_SIZES = [1, 7, 8, 9, 2047, 2048, 4095, 4096, 4097, 3 * 2048 + 1, 12345, 65536 + 24, 0, 300]
 
 
+@pytest.mark.parametrize("exact", MODES, ids=MODE_IDS)
 @pytest.mark.parametrize("sr", [1, 0])
-def test_edge_sizes_mixed_paths(cuda_device, sr):
+def test_edge_sizes_mixed_paths(cuda_device, sr, exact):
     """Ragged tails, partial blocks, the 4095/4096 routing edge and an empty
     tensor in one list, 4 steps, both rounding modes."""
     wl = W.custom("edges", EDGE_SIZES, steps=4, outlier_rate=0.01, outlier_factor=50.0, data_seed=77)
-    _run_full(wl, cuda_device, sr=sr)
+    _run_full(wl, cuda_device, sr=sr, exact=exact)
 
 
-def test_zero_gradient_blocks(cuda_device):
+@pytest.mark.parametrize("exact", MODES, ids=MODE_IDS)
+def test_zero_gradient_blocks(cuda_device, exact):
     """Blocks whose moments are all zero (absmax 0, zero codes 127 and 0):
     zero gradients from the first step in some blocks, a whole tensor and a
     partial last block, and zero gradients again after nonzero steps, where the
@@ -91,10 +109,11 @@ def test_zero_gradient_blocks(cuda_device):
         grads[2].zero_()                                # a whole tensor
         if step >= 3:
             grads[3].zero_()                            # zero after nonzero steps
-    _run_full(wl, cuda_device, grad_hook=hook)
+    _run_full(wl, cuda_device, grad_hook=hook, exact=exact)
 
 
-def test_negative_zero_moments_and_params(cuda_device):
+@pytest.mark.parametrize("exact", MODES, ids=MODE_IDS)
+def test_negative_zero_moments_and_params(cuda_device, exact):
     """Signed zeros through the whole step, with beta1 = 0 so that the new
     first moment is 0*m + g.  Elements 0 mod 4 get a -0 gradient every step:
     their m is +0 (+0 + -0), so where the parameter starts at -0 (every third
@@ -114,7 +133,7 @@ def test_negative_zero_moments_and_params(cuda_device):
             g.view(torch.int16)[::4] = -32768
             if step % 2 == 0:
                 g.view(torch.int16)[2::4] = -32768
-    gpu, host = _run_full(wl, cuda_device, grad_hook=hook, param_hook=params_hook)
+    gpu, host = _run_full(wl, cuda_device, grad_hook=hook, param_hook=params_hook, exact=exact)
     # the cases are live: -0 parameters survive, and zero codes sit in blocks
     # whose absmax is nonzero
     for t in host:
@@ -184,7 +203,7 @@ def test_many_tensors_take_several_launches(cuda_device):
     _run_full(wl, cuda_device)
 
 
-def _run_bf16(wl, device, steps, offsets=None, sr=1):
+def _run_bf16(wl, device, steps, offsets=None, sr=1, exact=True):
     params = W.init_params(wl, device)
     offsets = offsets or [-1] * len(params)
     gpu = [q8.Tensor16(p, None, torch.zeros_like(p), torch.zeros_like(p), off) for p, off in zip(params, offsets)]
@@ -196,19 +215,29 @@ def _run_bf16(wl, device, steps, offsets=None, sr=1):
             a.grad = g
             b.grad = u16(g)
         h = hp_for(wl, step, sr)
-        q8.adamw_bf16_sr_step(gpu, q8.hparams(**h))
+        q8.adamw_bf16_sr_step(gpu, q8.hparams(**h, exact=int(exact)))
         o.adamw_bf16_sr_step(host, o.hparams(**h))
         torch.cuda.synchronize()
+        tol = None if exact else ParamTolerance()
         for i, (a, b) in enumerate(zip(gpu, host)):
             for name, x, y in (("param", a.param, b.param), ("m", a.m, b.m), ("v", a.v, b.v)):
-                np.testing.assert_array_equal(u16(x), y, err_msg="%s tensor %d step %d" % (name, i, step))
+                where = "%s tensor %d step %d" % (name, i, step)
+                if tol is not None and name == "param":
+                    tol.add(u16(x), y, where)
+                else:
+                    np.testing.assert_array_equal(u16(x), y, err_msg=where)
+        if tol is not None:
+            tol.check()
+            for a, b in zip(gpu, host):             # identical inputs for the next step
+                a.param.copy_(torch.from_numpy(b.param.view(np.int16)).view(torch.bfloat16).to(a.param.device))
 
 
 @pytest.mark.parametrize("sr", [1, 0])
-def test_bf16_state_full_parity(cuda_device, sr):
+@pytest.mark.parametrize("exact", MODES, ids=MODE_IDS)
+def test_bf16_state_full_parity(cuda_device, sr, exact):
     wl = W.custom("bf16", [1, 7, 2048, 2049, 5000, 1 << 18, 0, 333], steps=5, data_seed=82,
                   hp=dict(lr=1.2e-3, weight_decay=0.1), grad_std=1e-4)
-    _run_bf16(wl, cuda_device, 5, sr=sr)
+    _run_bf16(wl, cuda_device, 5, sr=sr, exact=exact)
 
 
 def test_bf16_state_misaligned_offsets(cuda_device):
@@ -241,13 +270,23 @@ def test_bad_arguments_raise(cuda_device):
 FULL = [("gpt2-350m", 0.01), ("gpt2-xl-1.5b", 0.005), ("gptneo-6.7b", 0.003), ("gptneo-2.7b-bf16", 0.003)]
 
 
+@pytest.mark.parametrize("exact", MODES, ids=MODE_IDS)
 @pytest.mark.parametrize("name,fraction", FULL)
-def test_full_size_sampled_parity(cuda_device, pool, name, fraction):
+def test_full_size_sampled_parity(cuda_device, pool, name, fraction, exact):
+    """The five configurations at full size over all their steps, launched as
+    the benchmark launches them: sampled blocks replayed by the oracle.  In the
+    fast mode (each side on its own trajectory) codes, absmax and BF16 moments
+    stay bit-exact and at least 99.9 % of the sampled parameters too; the
+    one-ulp bound of a single step is tested from identical inputs in
+    test_gpu_fast_mode.py and in the small cases above."""
     wl = W.WORKLOADS[name]
-    run = SampledRun(wl, cuda_device, fraction)
+    run = SampledRun(wl, cuda_device, fraction, exact=exact)
     run.run()
     compared = run.check(pool)
     assert compared > 0
+    if run.tol is not None:
+        print("%s fast mode: %d of %d sampled parameters differ from the oracle (largest distance %d ulp)" % (
+            name, run.tol.diff, run.tol.n, run.tol.max_ulps))
 
 
 @pytest.mark.parametrize("state", ["8bit", "bf16"])
@@ -282,7 +321,7 @@ def test_sharded_step_equals_unsharded(cuda_device, world):
     for step in range(1, 4):
         grads = W.make_grads(wl, step, cuda_device)
         hd = hp_for(wl, step)
-        h = q8.hparams(**hd)
+        h = q8.hparams(**hd, exact=1)
         for a, b, c, g in zip(whole, split, host, grads):
             a.grad = g
             b.grad = g
@@ -337,7 +376,7 @@ def test_packed_sqrt_division_guard_boundaries(cuda_device):
         host.grad = g
         gpu.grad = torch.from_numpy(g.view(np.int16)).to(dev).view(torch.bfloat16)
         h = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=step, seed=21, sr=1)
-        q8.adamw8bit_sr_step([gpu], q8.hparams(**h))
+        q8.adamw8bit_sr_step([gpu], q8.hparams(**h, exact=1))
         o.adamw8bit_sr_step([host], o.hparams(**h))
         torch.cuda.synchronize()
         compare_state8(gpu, host, "step %d" % step)
@@ -366,7 +405,7 @@ def test_bf16_state_guard_boundaries(cuda_device):
         host.grad = g
         gpu.grad = t(g)
         h = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.01, step=step, seed=22, sr=1)
-        q8.adamw_bf16_sr_step([gpu], q8.hparams(**h))
+        q8.adamw_bf16_sr_step([gpu], q8.hparams(**h, exact=1))
         o.adamw_bf16_sr_step([host], o.hparams(**h))
         torch.cuda.synchronize()
         for name, a, b in (("param", gpu.param, host.param), ("m", gpu.m, host.m), ("v", gpu.v, host.v)):

@@ -44,7 +44,7 @@ def adamw8(seed, sizes, out):
     for t in range(1, STEPS + 1):
         for a, g in zip(gpu, grads[t - 1]):
             a.grad = g
-        q8.adamw8bit_sr_step(gpu, q8.hparams(**hp_for(wl, t)), stream)
+        q8.adamw8bit_sr_step(gpu, q8.hparams(**hp_for(wl, t), exact=1), stream)
     stream.synchronize()
     for t in range(1, STEPS + 1):
         for b, g in zip(host, grads[t - 1]):
@@ -68,7 +68,7 @@ def other(seed, out):
     for t in range(1, STEPS + 1):
         t16.grad = grads[t - 1]
         t1.grad = grads[t - 1]
-        q8.adamw_bf16_sr_step([t16], q8.hparams(**hp_for(wl, t)), stream)
+        q8.adamw_bf16_sr_step([t16], q8.hparams(**hp_for(wl, t), exact=1), stream)
         q8.lion8bit_sr_step([t1], q8.lion_hparams(lr=1e-4, weight_decay=0.1, step=t, seed=3), stream)
     stream.synchronize()
     for t in range(1, STEPS + 1):
