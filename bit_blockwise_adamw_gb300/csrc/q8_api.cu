@@ -67,6 +67,7 @@ int make_scalars(const q8_adamw_hparams* hp, q8::Scalars* s)
     s->fast_div = (s->eps_t >= 0x1p-100f && s->eps_t <= 0x1p20f) ? 1 : 0;
     s->approx = (hp->exact == 0 && s->eps_t >= 0x1p-36f && s->eps_t <= 0x1p20f && s->step_size <= 1.0f) ? 1 : 0;
     s->cancel = s->step_size * 0x1p-9f;
+    s->two16 = 65536u;
     return Q8_OK;
 }
 

@@ -13,6 +13,12 @@ __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w <
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 // The two bf16 values of one word as (low element, high element).
 __device__ __forceinline__ float2 bf16x2(uint32_t w) { return make_float2(bf16lo(w), bf16hi(w)); }
+// The same, the low half moved up by a multiply with two16 = 65536 passed in
+// from the host (an integer multiply-add, on the FMA pipe) instead of a shift.
+__device__ __forceinline__ float2 bf16x2_fma(uint32_t w, uint32_t two16)
+{
+    return make_float2(__uint_as_float(w * two16), bf16hi(w));
+}
 
 // ---------------------------------------------------------------- Philox
 // Philox4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11): ten rounds of

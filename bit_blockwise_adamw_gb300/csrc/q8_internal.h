@@ -70,6 +70,9 @@ struct Scalars {
                                // step_size <= 1: the full blocks' parameter update may use
                                // the approximate square root and reciprocal (ratio2_approx)
     float cancel;              // step_size * 2^-9: the cancellation bound of the fast mode
+    uint32_t two16;            // 65536, from the host: the AdamW kernel's low-half bf16
+                               // unpack is a multiply by it, which runs on the FMA pipe
+                               // (a shift would load the busier ALU pipe)
 };
 
 // Tensor lists travel as kernel parameters (no device allocation, no copy):

@@ -293,7 +293,7 @@ __device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int
             m[k] = __fmul2_rn(make_float2(sm.cs[byte_of(cw, b0)], sm.cs[byte_of(cw, b0 + 1)]), Mold);
             v[k] = __fmul2_rn(make_float2(sm.cu[byte_of(vw, b0)], sm.cu[byte_of(vw, b0 + 1)]), Vold);
         }
-        moments2(s, bf16x2(f.g[k]), m[k], v[k]);
+        moments2(s, bf16x2_fma(f.g[k], s.two16), m[k], v[k]);
     }
     if constexpr (!FULL) {
         // padding elements do not count in the block absmax
@@ -320,7 +320,7 @@ __device__ __forceinline__ void block_step(const Scalars& s, const Desc8& d, int
 #pragma unroll
             for (int j = 0; j < 2; ++j) {
                 const float2 q = ratio2_approx(s, m[k0 + j], v[k0 + j]);
-                x[j] = step2(s, bf16x2(f.p[k0 + j]), q);
+                x[j] = step2(s, bf16x2_fma(f.p[k0 + j], s.two16), q);
                 const float2 t = __fmul2_rn(q, splat(s.cancel));
                 redo = redo | (fabsf(x[j].x) < fabsf(t.x)) | (fabsf(x[j].y) < fabsf(t.y));
             }
