@@ -77,11 +77,13 @@ enum {
  * everywhere, so that every output is bit-identical with the plain CPU
  * restatement of these formulas.  exact = 0 (the fast mode) lets the full
  * 2048-blocks of the 8-bit and BF16-state kernels take them from the
- * hardware's approximate square root and reciprocal (when eps_t lies in
- * [2^-100, 2^20]; otherwise exact).  Both feed only the parameter update, so
- * codes, absmax and the BF16 m and v are identical in both modes; a parameter
- * differs only where the approximation moves its BF16 rounding, by one ulp
- * on a few elements in a million per step.
+ * hardware's approximate square root and reciprocal, when eps_t lies in
+ * [2^-36, 2^20] and a_t <= 1 (otherwise the step is exact).  Both feed only
+ * the parameter update, so codes, absmax and the BF16 m and v are identical
+ * in both modes.  A parameter differs only where the approximation moves its
+ * BF16 rounding: elements whose update nearly cancels p*decay are recomputed
+ * exactly, so a step's parameters are within one ulp of the exact step's,
+ * and about one in a million differs.
  * Any other value of sr or exact is an argument error.
  */
 typedef struct {
