@@ -30,14 +30,14 @@ def pool():
 
 
 def _run_full(wl, device, steps=None, sr=1, offsets=None, split=None, grad_hook=None, param_hook=None, shifted=(),
-              exact=True):
+              exact=True, expect_bitexact=False):
     """Run `wl` on both sides for `steps`, comparing everything after each step
     (`grad_hook(step, grads)` may edit the step's gradients in place first,
     `param_hook(params)` the initial parameters; the params and grads of the
     tensors in `shifted` sit 16 bytes past a 32-byte boundary).  exact=False
     runs the fast mode and holds the parameters of each step to its tolerance,
     then gives the GPU the oracle's parameters, so that every step starts from
-    identical inputs."""
+    identical inputs (expect_bitexact: the fast mode must be bit-exact here)."""
     steps = steps or wl.steps
     params = W.init_params(wl, device)
     params = [shift16(p) if i in shifted else p for i, p in enumerate(params)]
@@ -61,7 +61,7 @@ def _run_full(wl, device, steps=None, sr=1, offsets=None, split=None, grad_hook=
             q8.adamw8bit_sr_step(gpu, q8.hparams(**h, exact=int(exact)))
         o.adamw8bit_sr_step(host, o.hparams(**h))
         torch.cuda.synchronize()
-        tol = None if exact else ParamTolerance()
+        tol = None if exact or expect_bitexact else ParamTolerance()
         for i, (a, b) in enumerate(zip(gpu, host)):
             compare_state8(a, b, "tensor %d step %d" % (i, step), tol)
         if tol is not None:
@@ -93,6 +93,15 @@ def test_edge_sizes_mixed_paths(cuda_device, sr, exact):
     tensor in one list, 4 steps, both rounding modes."""
     wl = W.custom("edges", EDGE_SIZES, steps=4, outlier_rate=0.01, outlier_factor=50.0, data_seed=77)
     _run_full(wl, cuda_device, sr=sr, exact=exact)
+
+
+@pytest.mark.parametrize("hp", [dict(eps=0.0), dict(eps=1e-12), dict(lr=10.0, weight_decay=0.0)],
+                         ids=["eps_zero", "eps_below_2^-36", "step_size_above_1"])
+def test_fast_mode_outside_its_range_is_exact(cuda_device, hp):
+    """The fast mode applies only for eps_t in [2^-36, 2^20] and a_t <= 1;
+    outside that range a call with exact=0 takes the exact path, bit for bit."""
+    wl = W.custom("fastrange", [2048 * 6, 2048 * 2 + 7, 5000], steps=3, data_seed=96, hp=hp)
+    _run_full(wl, cuda_device, exact=False, expect_bitexact=True)
 
 
 @pytest.mark.parametrize("exact", MODES, ids=MODE_IDS)
