@@ -36,7 +36,12 @@ std::string at(const char* what, int i)
 }
 
 // Step scalars: formed in double from the hyper-parameters, rounded once to
-// float.  beta^t is libm pow in double.
+// float.  beta^t is libm pow in double.  The fast mode (exact = 0) is taken
+// only where its error bound holds: eps_t in [2^-36, 2^20] keeps the
+// approximate reciprocal's argument normal and a subnormal v (flushed to zero)
+// below half an ulp of eps_t; a_t <= 1 keeps the absolute error of a
+// subnormal quotient, times a_t, below one fp32 step of the parameter
+// (ratio2_approx).
 int make_scalars(const q8_adamw_hparams* hp, q8::Scalars* s)
 {
     if (!hp) return fail(Q8_ERR_NULL, "hparams is NULL");

@@ -8,8 +8,11 @@
 // blocks with vector loads and stores only, then the tensor's partial last
 // block with per-element bounds.  Each thread owns eight contiguous elements
 // and draws three independent Philox streams (p, m, v).
-// The square root and division take the packed exact path when all of a
-// thread's eight elements lie inside its bounds (q8_device.cuh).
+// In the fast mode the full blocks take the approximate square root and
+// reciprocal (ratio2_approx) unless the thread's cancellation check fails;
+// otherwise, and in the bit-exact mode, the square root and division take the
+// packed exact path when all of a thread's eight elements lie inside its
+// bounds (q8_device.cuh), the IEEE operations when not.
 #include "q8_device.cuh"
 
 namespace q8 {
