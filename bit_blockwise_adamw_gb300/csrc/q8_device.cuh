@@ -99,6 +99,16 @@ __device__ __forceinline__ uint32_t rne_hi(float x)
 // Top halves of a and b -> (b_hi << 16) | a_hi.
 __device__ __forceinline__ uint32_t pack_hi(uint32_t a, uint32_t b) { return __byte_perm(a, b, 0x7632); }
 
+// The same for a pair known to hold no NaN (infinities are fine: the add
+// cannot carry out of them), without the quieting.
+template <bool SR>
+__device__ __forceinline__ uint32_t round2_num(float2 x, uint32_t r)
+{
+    const uint32_t ux = __float_as_uint(x.x), uy = __float_as_uint(x.y);
+    if constexpr (SR) return pack_hi(ux + (r & 0xFFFFu), uy + (r >> 16));
+    else return pack_hi(ux + 0x7FFFu + ((ux >> 16) & 1u), uy + 0x7FFFu + ((uy >> 16) & 1u));
+}
+
 // Round a pair to bf16 and pack it into one word (draws in r: low half for
 // the first element, high half for the second).
 template <bool SR>

@@ -95,6 +95,27 @@ def test_edge_sizes_mixed_paths(cuda_device, sr, exact):
     _run_full(wl, cuda_device, sr=sr, exact=exact)
 
 
+@pytest.mark.parametrize("exact", MODES, ids=MODE_IDS)
+@pytest.mark.parametrize("sr", [1, 0])
+def test_nonfinite_parameters(cuda_device, sr, exact):
+    """NaN, +inf and -inf parameters (finite gradients) in full blocks, a
+    partial block and the fp32-state path: the step keeps the infinities and
+    writes the quiet NaN 0x7FC0, as the oracle does, in both modes (the fast
+    mode sends a NaN to its IEEE fallback; its one-ulp tolerance admits no other
+    pattern for a NaN or an infinity)."""
+    wl = W.custom("nonfinite", [2048 * 4, 2048 * 2 + 100, 3000], steps=3, data_seed=97)
+
+    def params_hook(params):
+        for p in params:
+            w = p.view(torch.int16)
+            w[5::97] = 0x7FC0                      # NaN
+            w[11::89] = 0x7F80                     # +inf
+            w[17::83] = -128                       # -inf (0xFF80)
+    gpu, host = _run_full(wl, cuda_device, sr=sr, param_hook=params_hook, exact=exact)
+    for t in host:
+        assert int((t.param == 0x7FC0).sum()) > 0 and int((t.param == 0x7F80).sum()) > 0
+
+
 @pytest.mark.parametrize("hp", [dict(eps=0.0), dict(eps=1e-12), dict(lr=10.0, weight_decay=0.0)],
                          ids=["eps_zero", "eps_below_2^-36", "step_size_above_1"])
 def test_fast_mode_outside_its_range_is_exact(cuda_device, hp):
