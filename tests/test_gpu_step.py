@@ -178,15 +178,16 @@ def test_explicit_misaligned_offsets(cuda_device):
     _run_full(wl, cuda_device, offsets=[3, 1 << 33, 12345677, 7])
 
 
+@pytest.mark.parametrize("exact", MODES, ids=MODE_IDS)
 @pytest.mark.parametrize("sr", [1, 0])
 @pytest.mark.parametrize("shifted", [(0, 1, 2, 3), (2,)], ids=["all", "one"])
-def test_grad_and_param_16_byte_aligned(cuda_device, sr, shifted):
+def test_grad_and_param_16_byte_aligned(cuda_device, sr, shifted, exact):
     """Grad and param arrays 16-byte but not 32-byte aligned (all of them, or
     one tensor of the list): the launch then moves grad and param with 16-byte
     accesses instead of 32-byte ones; the results are the oracle's all the same."""
     sizes = [2048 * 40, 2048 * 7 + 5, 5000, 1000]
     wl = W.custom("shift16", sizes, steps=3, data_seed=83, grad_std=1e-3)
-    _run_full(wl, cuda_device, sr=sr, shifted=shifted)
+    _run_full(wl, cuda_device, sr=sr, shifted=shifted, exact=exact)
 
 
 def test_split_list_equals_whole_list(cuda_device):
@@ -377,6 +378,33 @@ def test_sharded_step_equals_unsharded(cuda_device, world):
             assert torch.equal(a.m_absmax, b.m_absmax) and torch.equal(a.v_absmax, b.v_absmax)
         else:
             assert torch.equal(a.m32, b.m32) and torch.equal(a.v32, b.v32)
+
+
+@pytest.mark.parametrize("world", [3, 8])
+def test_sharded_fast_step_equals_unsharded(cuda_device, world):
+    """The fast mode shards like the bit-exact one: each element's result
+    depends only on that element (and the cancellation check on its own pair),
+    so N ranks' block-aligned slices with global Philox offsets give the
+    unsharded fast step's bits."""
+    from bit_blockwise_adamw_gb300 import sharding
+    wl = W.custom("shard", [2048 * 50 + 7, 300, 4096, 2048 * 9, 1000, 65536 + 24], steps=3, data_seed=84)
+    params = W.init_params(wl, cuda_device)
+    whole = gpu_states8([p.clone() for p in params])
+    split = gpu_states8([p.clone() for p in params])
+    for step in range(1, 4):
+        grads = W.make_grads(wl, step, cuda_device)
+        h = q8.hparams(**hp_for(wl, step), exact=0)
+        for a, b, g in zip(whole, split, grads):
+            a.grad = g
+            b.grad = g
+        q8.adamw8bit_sr_step(whole, h)
+        for rank in range(world):
+            q8.adamw8bit_sr_step(sharding.shard(split, world, rank), h)
+        torch.cuda.synchronize()
+        for a, b in zip(whole, split):
+            for f in ("param", "m_codes", "v_codes", "m_absmax", "v_absmax", "m32", "v32"):
+                x, y = getattr(a, f), getattr(b, f)
+                assert x is None or torch.equal(x.view(torch.uint8), y.view(torch.uint8)), (f, step)
 
 
 def test_packed_sqrt_division_guard_boundaries(cuda_device):
