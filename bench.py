@@ -511,7 +511,7 @@ def _time_steps(fn, steps, warmup, stream, device, barrier):
 
 def run_secondary(args, wl8, states8, peak, device, world, barrier):
     """The headline's 8-bit AdamW step in its other mode (bit-exact or fast),
-    BF16-state AdamW on the GPT-Neo 2.7B list (in the headline's mode), 8-bit
+    BF16-state AdamW on the GPT-Neo 2.7B list (in both modes), 8-bit
     Momentum and 8-bit Lion on the 6.7B list (using the headline's parameters,
     gradients and state), each with the headline's warm-up and events, one
     launch per step.  Per entry: ms/step, Gparams/s, algorithmic GB/s and the
@@ -569,6 +569,11 @@ def run_secondary(args, wl8, states8, peak, device, world, barrier):
         step=t, seed=wl16.philox_seed, exact=int(args.exact)), stream), args.secondary_steps, args.warmup, stream,
         device, barrier)
     entry("adamw_bf16", wl16, "step16_kernel", 2, per, launches_per_step(wl16))
+    per = _time_steps(lambda t: q8.adamw_bf16_sr_step(packed16, q8.hparams(
+        lr=h16["lr"], beta1=h16["beta1"], beta2=h16["beta2"], eps=h16["eps"], weight_decay=h16["weight_decay"],
+        step=t, seed=wl16.philox_seed, exact=other), stream), args.secondary_steps, args.warmup, stream,
+        device, barrier)
+    entry("adamw_bf16_exact" if other else "adamw_bf16_fast", wl16, "step16_kernel", 2, per, launches_per_step(wl16))
     del st16, packed16, p16, g16
     torch.cuda.empty_cache()
     return out
