@@ -9,6 +9,8 @@ same 16-bit stochastic-rounding draw (bits + r, keep the top half) or to
 nearest even, land at most one bf16 ulp apart.  Checked here on random pairs
 spread over the whole exponent range, on pairs placed at binade edges and at
 the largest allowed distance, and with every draw for a few fixed pairs.
+The quotient bound the cancellation check rests on (within 2^-19 of the
+correctly rounded quotient) is checked by emulation too.
 """
 import numpy as np
 
@@ -79,3 +81,28 @@ def test_the_bound_is_needed():
     a = np.full(r.size, 1.3, np.float32)
     b = (a.astype(np.float64) * (1.0 + 2.0 ** -6)).astype(np.float32)
     assert np.abs(_sr(a.view(np.uint32), r) - _sr(b.view(np.uint32), r)).max() >= 2
+
+
+def test_quotient_error_bound():
+    """The other half of the argument: with the approximate square root and
+    reciprocal each within 2^-21 relative error (the device self-test measures
+    about 2^-23.3), and the packed add and multiply rounded to fp32, the fast
+    quotient m * rcp(sqrt(v) + eps_t) lies within 2^-19 of the correctly rounded
+    m / (sqrt(v) + eps_t).  Emulated in float64 with the roundings to fp32 at
+    the same places, the approximation errors at their extremes."""
+    rng = np.random.default_rng(13)
+    n = 2_000_000
+    f32 = lambda x: np.asarray(x, np.float64).astype(np.float32).astype(np.float64)
+    v = f32(np.exp2(rng.uniform(-126, 120, n)))
+    m = f32(np.exp2(rng.uniform(-120, 60, n)) * np.where(rng.integers(0, 2, n) == 1, -1.0, 1.0))
+    eps = f32(np.exp2(rng.uniform(-36, 20, n)))
+    exact = f32(m / f32(f32(np.sqrt(v)) + eps))
+    es = rng.choice([-1.0, 1.0], n) * 2.0 ** -21
+    er = rng.choice([-1.0, 1.0], n) * 2.0 ** -21
+    s_a = f32(np.sqrt(v) * (1.0 + es))
+    d_a = f32(s_a + eps)
+    y_a = f32((1.0 / d_a) * (1.0 + er))
+    fast = f32(m * y_a)
+    ok = np.isfinite(exact) & (np.abs(exact) >= 2.0 ** -126)    # normal quotients
+    rel = np.abs(fast[ok] - exact[ok]) / np.abs(exact[ok])
+    assert rel.max() <= 2.0 ** -19
