@@ -111,7 +111,7 @@ def metrics(d, r):
                 unmoved=float(np.count_nonzero((d == 0) & moved)) / max(int(np.count_nonzero(moved)), 1))
 
 
-def run(regime, seed, steps, device, every=None):
+def run(regime, seed, steps, device, every=None, exact=1):
     """One regime and seed.  Returns {step: {(arm, rounding): metrics}} at the
     checkpoints (every `every` steps, and the last)."""
     cfg = REGIMES[regime]
@@ -154,7 +154,7 @@ def run(regime, seed, steps, device, every=None):
         host_g.numpy()[:] = gb.view(np.int16)
         grad.view(torch.int16).copy_(host_g)
         for name, sr in ROUNDINGS.items():
-            hp = q8.hparams(exact=1, lr=cfg["lr"], beta1=B1, beta2=B2, eps=EPS, weight_decay=cfg["wd"],
+            hp = q8.hparams(exact=exact, lr=cfg["lr"], beta1=B1, beta2=B2, eps=EPS, weight_decay=cfg["wd"],
                             step=t, seed=seed, sr=sr)
             q8.adamw8bit_sr_step(lists8[name], hp)
             q8.adamw_bf16_sr_step(lists16[name], hp)
@@ -195,6 +195,7 @@ def main():
     ap.add_argument("--seeds", type=int, default=3)
     ap.add_argument("--every", type=int, default=500)
     ap.add_argument("--regimes", nargs="*", default=list(REGIMES))
+    ap.add_argument("--fast", action="store_true", help="the AdamW steps in the fast mode (default: bit-exact)")
     a = ap.parse_args()
     dev = torch.device("cuda", 0)
     results = {}
@@ -202,13 +203,14 @@ def main():
     for regime in a.regimes:
         results[regime] = {}
         for seed in range(1, a.seeds + 1):
-            results[regime][seed] = run(regime, seed, a.steps, dev, a.every)
+            results[regime][seed] = run(regime, seed, a.steps, dev, a.every, exact=0 if a.fast else 1)
             for t, row in results[regime][seed].items():
                 print("%s seed %d step %d: %s" % (regime, seed, t, "; ".join(
                     "%s/%s %.3f %.3f" % (arm, name, m["realised"], m["rel_err"]) for (arm, name), m in row.items())),
                       flush=True)
     print()
-    print("%d steps, seeds 1..%d, %.0f s" % (a.steps, a.seeds, time.time() - t0))
+    print("%d steps, seeds 1..%d, %s mode, %.0f s" % (a.steps, a.seeds, "fast" if a.fast else "bit-exact",
+                                                     time.time() - t0))
     print(table(results, a.steps))
 
 
